@@ -1,0 +1,411 @@
+"""Seeded synthetic decode-step workloads (input generation only).
+
+Each builder returns the host-side state a block manager hands to the
+kernels for one decode step: sequence lengths, block tables, the slot of
+every new token and the copy-on-write pairs. Values (Q, the new K/V and the
+pool contents) are drawn by ``make_values``. Nothing here computes
+attention, writes the cache or copies blocks.
+
+The tables come from a small LIFO free-list simulation (``_Tables``) that
+mirrors how a paged block manager hands out blocks: a block is taken when
+the previous one is full ("03 · PagedAttention", "Blocks and block tables"),
+blocks are uniform so a free list suffices ("PagedAttention", "Pros"), and
+a write into a shared block first takes a copy ("PagedAttention",
+copy-on-write diagram). Every workload also carries an operation log so
+that an independent allocator can replay it and must reach the same tables.
+
+Length conventions: ``seq_lens[s]`` is the number of tokens attended in the
+step, including the new token, which sits at position ``seq_lens[s] - 1``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+PAD = -1  # table entries past a sequence's last block
+
+
+@dataclass
+class Workload:
+    name: str
+    num_seqs: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    seq_lens: np.ndarray        # int32 [S], attended lengths
+    block_tables: np.ndarray    # int32 [S, max_blocks], PAD beyond each table
+    slot_mapping: np.ndarray    # int32 [S], slot of each sequence's new token
+    cow_pairs: np.ndarray       # int32 [n_pairs, 2] (src, dst)
+    free_order: np.ndarray      # int32 [num_blocks], initial hand-out order
+    ops: list = field(default_factory=list)  # replayable allocator log
+    seed: int = 0
+    partition_tokens: int = 0   # 0: let the library choose
+    note: str = ""
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.num_seqs else 0
+
+    @property
+    def group(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+    @property
+    def tokens_attended(self) -> int:
+        return int(self.seq_lens.astype(np.int64).sum())
+
+    def kv_bytes(self, elem_bytes: int = 2) -> int:
+        """K+V bytes one decode step must read: sum_s len_s * Hkv * d * 2 (K,V)."""
+        return self.tokens_attended * self.n_kv_heads * self.head_dim * elem_bytes * 2
+
+    def io_bytes(self, elem_bytes: int = 2) -> int:
+        """Non-KV bytes of one decode: q, out, the tables actually read, lengths."""
+        S, Hq, d = self.num_seqs, self.n_q_heads, self.head_dim
+        nblk = int(np.sum((self.seq_lens.astype(np.int64) + self.block_size - 1)
+                          // self.block_size))
+        return 2 * S * Hq * d * elem_bytes + 4 * nblk + 4 * S
+
+
+class _Tables:
+    """Minimal LIFO block hand-out used only to build synthetic tables."""
+
+    def __init__(self, free_order, block_size):
+        self.bs = block_size
+        self.stack = list(np.asarray(free_order, dtype=np.int64)[::-1])
+        self.ref = {}
+        self.tables = []
+        self.lens = []
+        self.alive = []
+        self.ops = []
+
+    def _pop(self):
+        if not self.stack:
+            raise RuntimeError("synthetic pool exhausted")
+        b = int(self.stack.pop())
+        self.ref[b] = 1
+        return b
+
+    def add(self):
+        self.tables.append([])
+        self.lens.append(0)
+        self.alive.append(True)
+        self.ops.append(("add",))
+        return len(self.tables) - 1
+
+    def grow(self, s, n):
+        """Append n tokens to s; its last block must not be shared."""
+        if n <= 0:
+            return
+        L = self.lens[s]
+        need = -(-(L + n) // self.bs) - len(self.tables[s])
+        if L % self.bs and self.ref[self.tables[s][-1]] > 1:
+            raise RuntimeError("grow() into a shared block")
+        if need > len(self.stack):
+            raise RuntimeError("synthetic pool exhausted")
+        for _ in range(need):
+            self.tables[s].append(self._pop())
+        self.lens[s] = L + n
+        self.ops.append(("append", s, n))
+
+    def fork(self, s):
+        t = list(self.tables[s])
+        for b in t:
+            self.ref[b] += 1
+        self.tables.append(t)
+        self.lens.append(self.lens[s])
+        self.alive.append(True)
+        self.ops.append(("fork", s))
+        return len(self.tables) - 1
+
+    def free(self, s):
+        for b in reversed(self.tables[s]):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                del self.ref[b]
+                self.stack.append(b)
+        self.tables[s] = []
+        self.lens[s] = 0
+        self.alive[s] = False
+        self.ops.append(("free", s))
+
+    def step(self, s):
+        """The decode step's one new token: returns (slot, cow pair or None)."""
+        L = self.lens[s]
+        pair = None
+        if L % self.bs == 0:
+            self.tables[s].append(self._pop())
+        else:
+            j = L // self.bs
+            old = self.tables[s][j]
+            if self.ref[old] > 1:
+                new = self._pop()
+                self.ref[old] -= 1
+                self.tables[s][j] = new
+                pair = (old, new)
+        self.lens[s] = L + 1
+        self.ops.append(("step", s))
+        blk = self.tables[s][L // self.bs]
+        return blk * self.bs + L % self.bs, pair
+
+
+def _finish(name, tb: _Tables, seqs, free_order, *, Hq, Hkv, d, num_blocks, seed,
+            slots, pairs, partition_tokens=0, note=""):
+    lens = np.array([tb.lens[s] for s in seqs], dtype=np.int32)
+    maxb = max(1, max((len(tb.tables[s]) for s in seqs), default=1))
+    bt = np.full((len(seqs), maxb), PAD, dtype=np.int32)
+    for i, s in enumerate(seqs):
+        bt[i, :len(tb.tables[s])] = tb.tables[s]
+    cp = np.array(pairs, dtype=np.int32).reshape(-1, 2)
+    return Workload(name=name, num_seqs=len(seqs), n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d,
+                    block_size=tb.bs, num_blocks=num_blocks, seq_lens=lens, block_tables=bt,
+                    slot_mapping=np.array(slots, dtype=np.int32), cow_pairs=cp,
+                    free_order=np.asarray(free_order, dtype=np.int32), ops=tb.ops,
+                    seed=seed, partition_tokens=partition_tokens, note=note)
+
+
+def _two_phase(name, lens, *, bs, num_blocks, Hq, Hkv, d, seed, rng, partition_tokens=0,
+               note=""):
+    """Sequences with L-1 cached tokens each (taken in sequence order from a
+    shuffled free list), then the step appends token L-1 to each in turn."""
+    free_order = rng.permutation(num_blocks)
+    tb = _Tables(free_order, bs)
+    seqs = [tb.add() for _ in lens]
+    for s, L in zip(seqs, lens):
+        tb.grow(s, int(L) - 1)
+    slots, pairs = [], []
+    for s in seqs:
+        slot, pair = tb.step(s)
+        slots.append(slot)
+        if pair:
+            pairs.append(pair)
+    return _finish(name, tb, seqs, free_order, Hq=Hq, Hkv=Hkv, d=d, num_blocks=num_blocks,
+                   seed=seed, slots=slots, pairs=pairs, partition_tokens=partition_tokens,
+                   note=note)
+
+
+def _lognormal_lengths(rng, n, median, sigma, lo, hi):
+    z = rng.standard_normal(n)
+    return np.clip(np.rint(np.exp(np.log(median) + sigma * z)), lo, hi).astype(np.int64)
+
+
+# ------------------------------------------------------------------ configs
+
+WORKED_EXAMPLE_LENGTHS = (512, 37, 1900, 128, 4)
+
+
+def config1(seed: int = 1) -> Workload:
+    """Worked example: lengths 512/37/1900/128/4, block 16, a 256-block pool
+    handed out in a seeded random order, 8 q / 8 kv heads, head_dim 64."""
+    rng = np.random.default_rng(seed)
+    return _two_phase("worked-example-5seq-bs16-mha8-d64", WORKED_EXAMPLE_LENGTHS, bs=16,
+                      num_blocks=256, Hq=8, Hkv=8, d=64, seed=seed, rng=rng)
+
+
+def config2(seed: int = 2, num_seqs: int = 64, block_size: int = 16) -> Workload:
+    """GQA decode batch: 64 sequences, lengths lognormal (median 300, sigma 1,
+    clipped to [1, 2048]), 32 q / 8 kv heads, head_dim 128, pool 1.25x need."""
+    rng = np.random.default_rng(seed)
+    lens = _lognormal_lengths(rng, num_seqs, 300.0, 1.0, 1, 2048)
+    need = int(sum(-(-int(L) // block_size) for L in lens))
+    nb = int(math.ceil(1.25 * need))
+    return _two_phase(f"gqa-decode-{num_seqs}seq-lognorm300-bs{block_size}-q32kv8-d128", lens,
+                      bs=block_size, num_blocks=nb, Hq=32, Hkv=8, d=128, seed=seed, rng=rng)
+
+
+def config3(block_size: int = 16, seed: int = 3, num_seqs: int = 256, max_len: int = 4096,
+            n_heads: int = 32, phantoms: int = 512) -> Workload:
+    """MHA decode over a fragmented pool: lengths uniform on [1, max_len];
+    32 q = 32 kv heads, head_dim 128; the tables come from a free list after
+    churn: phantom sequences grow round-robin until the pool is ~90% full, a
+    seeded half of them is freed, then the real sequences grow round-robin,
+    freeing further phantoms (seeded order) whenever the pool runs dry."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, max_len + 1, size=num_seqs)
+    need = int(sum(-(-int(L) // block_size) for L in lens))
+    nb = int(math.ceil(1.25 * need)) + 64
+    free_order = np.arange(nb)
+    tb = _Tables(free_order, block_size)
+    ph_lens = rng.integers(1, max_len + 1, size=phantoms)
+    ph = [tb.add() for _ in range(phantoms)]
+    target = int(0.9 * nb)
+    used = 0
+    # Round-robin growth, one block-round at a time (token-round-robin takes
+    # blocks in exactly this order).
+    done = False
+    for b in range(-(-max_len // block_size)):
+        for s, L in zip(ph, ph_lens):
+            if used >= target:
+                done = True
+                break
+            lo = b * block_size
+            if lo < L:
+                tb.grow(s, min(int(L), lo + block_size) - lo)
+                used += 1
+        if done:
+            break
+    victims = list(rng.permutation(phantoms))
+    for s in victims[: phantoms // 2]:
+        tb.free(ph[s])
+    spare = victims[phantoms // 2:]
+    real = [tb.add() for _ in range(num_seqs)]
+    for b in range(-(-max_len // block_size)):
+        for s, L in zip(real, lens):
+            lo = b * block_size
+            hi = min(int(L) - 1, lo + block_size)  # L-1 tokens before the step
+            if lo < hi:
+                while not tb.stack:
+                    tb.free(ph[spare.pop(0)])
+                tb.grow(s, hi - lo)
+    slots, pairs = [], []
+    for s in real:
+        if tb.lens[s] % block_size == 0:
+            while not tb.stack:
+                tb.free(ph[spare.pop(0)])
+        slot, pair = tb.step(s)
+        slots.append(slot)
+        if pair:
+            pairs.append(pair)
+    return _finish(f"mha-decode-{num_seqs}seq-uniform{max_len}-bs{block_size}-h{n_heads}-d128"
+                   "-churned", tb, real, free_order, Hq=n_heads, Hkv=n_heads, d=128,
+                   num_blocks=nb, seed=seed, slots=slots, pairs=pairs)
+
+
+def config4(seed: int = 4, num_seqs: int = 128, prefix_tokens: int = 1024,
+            block_size: int = 16) -> Workload:
+    """Prefix sharing with copy-on-write: every sequence maps the same
+    1024-token prefix (64 blocks) and owns a suffix of lognormal length
+    (median 200, sigma 1, clipped to [1, 1024]). Each sequence has a sibling
+    fork taken before this step (as in parallel sampling or beam search), so
+    its partially filled last block is shared; the step's write into it
+    copies the block first. 32 q / 8 kv heads, head_dim 128."""
+    rng = np.random.default_rng(seed)
+    suffix = _lognormal_lengths(rng, num_seqs, 200.0, 1.0, 1, 1024)
+    pre_blocks = -(-prefix_tokens // block_size)
+    need = pre_blocks + int(sum(-(-(int(x)) // block_size) + 1 for x in suffix))
+    nb = int(math.ceil(1.25 * need))
+    free_order = rng.permutation(nb)
+    tb = _Tables(free_order, block_size)
+    root = tb.add()
+    tb.grow(root, prefix_tokens)
+    seqs = [tb.fork(root) for _ in range(num_seqs)]
+    tb.free(root)
+    for s, x in zip(seqs, suffix):
+        tb.grow(s, int(x) - 1)
+        tb.fork(s)  # sibling, not decoded in this step
+    slots, pairs = [], []
+    for s in seqs:
+        slot, pair = tb.step(s)
+        slots.append(slot)
+        if pair:
+            pairs.append(pair)
+    return _finish(f"prefix-share-cow-{num_seqs}seq-prefix{prefix_tokens}-q32kv8-d128", tb,
+                   seqs, free_order, Hq=32, Hkv=8, d=128, num_blocks=nb, seed=seed,
+                   slots=slots, pairs=pairs)
+
+
+def config5(seed: int = 5, num_seqs: int = 16, seq_len: int = 32768,
+            partition_tokens: int = 512) -> Workload:
+    """Long-context split-KV: 16 sequences of 32768 tokens, block 16, blocks
+    placed at random in a pool of 1.25x need, 64 q / 8 kv heads, head_dim 128,
+    KV partitions of 512 tokens."""
+    rng = np.random.default_rng(seed)
+    need = num_seqs * (-(-seq_len // 16))
+    nb = int(math.ceil(1.25 * need))
+    return _two_phase(f"long-context-{num_seqs}x{seq_len}-bs16-q64kv8-d128", [seq_len] * num_seqs,
+                      bs=16, num_blocks=nb, Hq=64, Hkv=8, d=128, seed=seed, rng=rng,
+                      partition_tokens=partition_tokens)
+
+
+def custom(lens, *, block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128, seed=0,
+           extra_blocks=8, partition_tokens=0, name="custom") -> Workload:
+    """Any lengths (0 allowed: no token, no write) in the two-phase layout."""
+    rng = np.random.default_rng(seed)
+    lens = [int(L) for L in lens]
+    need = sum(-(-L // block_size) for L in lens)
+    nb = max(1, need + extra_blocks)
+    free_order = rng.permutation(nb)
+    tb = _Tables(free_order, block_size)
+    seqs = [tb.add() for _ in lens]
+    for s, L in zip(seqs, lens):
+        tb.grow(s, L - 1)
+    slots, pairs = [], []
+    for s, L in zip(seqs, lens):
+        if L == 0:
+            slots.append(-1)
+            continue
+        slot, pair = tb.step(s)
+        slots.append(slot)
+        if pair:
+            pairs.append(pair)
+    return _finish(name, tb, seqs, free_order, Hq=n_q_heads, Hkv=n_kv_heads, d=head_dim,
+                   num_blocks=nb, seed=seed, slots=slots, pairs=pairs,
+                   partition_tokens=partition_tokens)
+
+
+CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+
+
+# ------------------------------------------------------------------ values
+
+BF16_NAN = 0x7FC0
+BF16_POS_INF = 0x7F80
+
+
+def make_values(wl: Workload, device="cpu", seed=None, poison_tails: bool = False):
+    """Draw Q, the new K/V and the pool contents, bf16 ~ N(0, 1), seeded.
+
+    Returns a dict of torch tensors on ``device``: q [S,Hq,d], k_new/v_new
+    [S,Hkv,d] (one new token per sequence), k_pool/v_pool [NB,Hkv,bs,d].
+    With ``poison_tails`` the slots past each sequence's last token in its
+    last block (and, for a copy-on-write pair, the source block's slots from
+    the new token on) hold NaN/Inf bit patterns: they must never reach an
+    output.
+    """
+    import torch
+
+    seed = wl.seed if seed is None else seed
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + 17)
+    S, Hq, Hkv, d, bs, NB = (wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                             wl.block_size, wl.num_blocks)
+    bf = torch.bfloat16
+    out = {
+        "q": torch.randn((S, Hq, d), generator=g, device=device, dtype=bf),
+        "k_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf),
+        "v_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf),
+        "k_pool": torch.randn((NB, Hkv, bs, d), generator=g, device=device, dtype=bf),
+        "v_pool": torch.randn((NB, Hkv, bs, d), generator=g, device=device, dtype=bf),
+    }
+    if poison_tails:
+        poison_blocks, poison_from = [], []
+        pair_src = {int(dst): int(src) for src, dst in wl.cow_pairs}
+        for s in range(S):
+            L = int(wl.seq_lens[s])
+            if L == 0:
+                continue
+            j = (L - 1) // bs
+            blk = int(wl.block_tables[s, j])
+            off = (L - 1) % bs
+            poison_blocks.append(blk)
+            poison_from.append(off + 1)
+            if blk in pair_src:
+                poison_blocks.append(pair_src[blk])
+                poison_from.append(off)
+        for blk, start in zip(poison_blocks, poison_from):
+            if start < bs:
+                for name, bits in (("k_pool", BF16_NAN), ("v_pool", BF16_POS_INF)):
+                    view = out[name].view(torch.int16)
+                    view[blk, :, start:, :] = bits - (1 << 16 if bits >= 1 << 15 else 0)
+    return out
