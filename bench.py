@@ -1,0 +1,488 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path over one batch: copy-on-write block copies,
+the new tokens' K/V writes, and the paged decode attention (split-KV with a
+log-sum-exp merge). The default workload is the GQA decode batch (64
+sequences, lognormal lengths with median 300 clipped to [1, 2048], block 16,
+32 query / 8 kv heads, head_dim 128, bf16). Its pools fit in L2, so the
+timed steps rotate through enough independent replicas of the inputs that
+each step reads cold data.
+
+Metric: KV bytes the step must read (sum of lengths x kv heads x head_dim x
+2 bytes x K,V) per second of device time, plus tokens attended per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 1..5] [--block-size 8|16|32]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-read HBM GB/s (% of peak), tokens attended/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+KERNEL_SOURCES = ["paged_kv_cache_105_gb300/csrc/pa_decode.cu",
+                  "paged_kv_cache_105_gb300/csrc/pa_ptx.cuh"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32])
+    p.add_argument("--partition-tokens", type=int, default=None)
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def build_workload(cfg, bs):
+    from paged_kv_cache_105_gb300 import workloads as W
+    if cfg == 3:
+        return W.config3(block_size=bs)
+    return W.CONFIGS[cfg]()
+
+
+def dist_init(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on this workload with the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    key = f"traffic_bytes_per_launch[{workload_name}]"
+    if kv.get("kernel_source_sha256") != kernel_hash() or key not in kv:
+        return None
+    return float(kv[key])
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        if j.get("hbm_gbs"):
+            return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_oracle_step(wl, vals_cpu, seqs):
+    """The oracle's copy -> write -> attention for the sequences `seqs`
+    (a bounded sample of the workload). Returns KV bytes of the sample."""
+    import numpy as np
+    from oracle import paref
+    bits = _bits
+    kp, vp = bits(vals_cpu["k_pool"]).copy(), bits(vals_cpu["v_pool"]).copy()
+    paref.copy_blocks(kp, vp, wl.cow_pairs)
+    paref.reshape_and_cache(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
+                            wl.slot_mapping)
+    rows = np.array([(s, h) for s in seqs for h in range(wl.n_q_heads)], np.int32)
+    paref.attention_paged(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
+                          wl.scale, rows=rows)
+    return int(wl.seq_lens[list(seqs)].astype(np.int64).sum()) * wl.n_kv_heads * \
+        wl.head_dim * 2 * 2
+
+
+def cpu_sample_seqs(wl, budget_tokens):
+    """Sequences (longest last) whose total length stays within a budget."""
+    import numpy as np
+    order = np.random.default_rng(0).permutation(wl.num_seqs)
+    picked, tot = [], 0
+    for s in order:
+        L = int(wl.seq_lens[s])
+        if picked and tot + L > budget_tokens:
+            continue
+        picked.append(int(s))
+        tot += L
+    return sorted(picked), tot
+
+
+def run_reference(args):
+    """The oracle as the reference arm, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = build_workload(args.config, args.block_size)
+    budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
+    seqs, tok = cpu_sample_seqs(wl, budget)
+    vals = W_make_values_subset(wl, seqs)
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"])
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"])
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "sample_seqs": len(seqs), "sample_tokens": tok},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{len(seqs)} of {wl.num_seqs} sequences "
+                                       f"({tok} tokens) per step, all query heads"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def W_make_values_subset(wl, seqs):
+    """A self-contained sub-workload holding only `seqs` (tables remapped
+    onto a compact pool), with values drawn for exactly those blocks, so the
+    CPU baseline never allocates the full pool on the host."""
+    import numpy as np
+    from paged_kv_cache_105_gb300 import workloads as W
+    bs = wl.block_size
+    pair_src = {int(d): int(s) for s, d in wl.cow_pairs}
+    need = []
+    for s in seqs:
+        nb = -(-int(wl.seq_lens[s]) // bs)
+        for b in wl.block_tables[s, :nb]:
+            need.append(int(b))
+            if int(b) in pair_src:
+                need.append(pair_src[int(b)])
+    ids = list(dict.fromkeys(need))
+    remap = {b: i for i, b in enumerate(ids)}
+    maxb = wl.block_tables.shape[1]
+    bt = np.full((len(seqs), maxb), -1, np.int32)
+    slots, pairs = [], []
+    for i, s in enumerate(seqs):
+        nb = -(-int(wl.seq_lens[s]) // bs)
+        bt[i, :nb] = [remap[int(b)] for b in wl.block_tables[s, :nb]]
+        sl = int(wl.slot_mapping[s])
+        slots.append(-1 if sl < 0 else remap[sl // bs] * bs + sl % bs)
+        last = int(wl.block_tables[s, (int(wl.seq_lens[s]) - 1) // bs]) if nb else -1
+        if last in pair_src:
+            pairs.append((remap[pair_src[last]], remap[last]))
+    sub = W.Workload(name=wl.name + "-sample", num_seqs=len(seqs), n_q_heads=wl.n_q_heads,
+                     n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, block_size=bs,
+                     num_blocks=max(1, len(ids)), seq_lens=wl.seq_lens[seqs].astype(np.int32),
+                     block_tables=bt, slot_mapping=np.array(slots, np.int32),
+                     cow_pairs=np.array(pairs, np.int32).reshape(-1, 2),
+                     free_order=np.arange(max(1, len(ids)), dtype=np.int32), seed=wl.seed)
+    vals = W.make_values(sub, device="cpu")
+    return {"wl": sub, "vals": vals, "seqs": list(range(len(seqs)))}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_105_gb300 import binding as B
+    from paged_kv_cache_105_gb300 import workloads as W
+
+    wl = build_workload(args.config, args.block_size)
+    P = wl.partition_tokens if args.partition_tokens is None else args.partition_tokens
+    P_res = B.pa_decode_partition_tokens(wl.num_seqs, wl.n_kv_heads, wl.block_size,
+                                         wl.max_seq_len, P)
+    base = W.make_values(wl, device=dev)
+    pool_bytes = 2 * base["k_pool"].numel() * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    replicas = max(1, math.ceil(3 * l2 / max(1, wl.kv_bytes())))
+    replicas = min(replicas, max(1, int(40e9 // max(1, pool_bytes))))
+    reps = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(replicas - 1)]
+    t = {"bt": torch.from_numpy(wl.block_tables).to(dev),
+         "sl": torch.from_numpy(wl.seq_lens).to(dev),
+         "sm": torch.from_numpy(wl.slot_mapping).to(dev),
+         "pairs": torch.from_numpy(np.ascontiguousarray(wl.cow_pairs.reshape(-1, 2))).to(dev)}
+    outs = [torch.empty_like(r["q"]) for r in reps]
+    wss = [B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                              wl.block_size, wl.max_seq_len, P, device=dev) for _ in reps]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_pairs = int(wl.cow_pairs.shape[0])
+    launches_per_step = 1 + (1 if n_pairs else 0) + (1 if wl.num_seqs else 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        r = reps[i % replicas]
+        if n_pairs:
+            B.pa_copy_blocks(r["k_pool"], r["v_pool"], t["pairs"], err_word=err)
+        B.pa_reshape_and_cache(r["k_new"], r["v_new"], r["k_pool"], r["v_pool"], t["sm"],
+                               err_word=err)
+        if ev is not None:
+            ev[0].record(stream)
+        B.pa_decode(outs[i % replicas], r["q"], r["k_pool"], r["v_pool"], t["bt"], t["sl"],
+                    wl.scale, max_seq_len=wl.max_seq_len, workspace=wss[i % replicas],
+                    partition_tokens=P, err_word=err)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # Warm up with continuous load long enough for the clock sampler to see it.
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    t_pre = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_pre < 1.0:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(k, dec_ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    # keep the load on a little past the timed region for the sampler
+    t_post = time.perf_counter()
+    while time.perf_counter() - t_post < 0.3:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    kv_bytes = wl.kv_bytes()
+    alg_bytes = kv_bytes + wl.io_bytes()
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    tokens_per_s = world * wl.tokens_attended * args.steps / (total_ms * 1e-3)
+
+    # ---- end to end through the public API, host buffers, copies timed
+    e2e_steps = args.e2e_steps or max(10, min(200, args.steps))
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            for k, v in base.items() if k in ("q", "k_new", "v_new")}
+    for k in host:
+        host[k].copy_(base[k].cpu())
+    host_idx = {"bt": torch.from_numpy(wl.block_tables).pin_memory(),
+                "sl": torch.from_numpy(wl.seq_lens).pin_memory(),
+                "sm": torch.from_numpy(wl.slot_mapping).pin_memory(),
+                "pairs": torch.from_numpy(np.ascontiguousarray(
+                    wl.cow_pairs.reshape(-1, 2))).pin_memory()}
+    host_out = torch.empty(base["q"].shape, dtype=torch.bfloat16, pin_memory=True)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dev_idx = {k: torch.empty_like(v, device=dev) for k, v in host_idx.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
+        sum(v.numel() * v.element_size() for v in host_idx.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(i):
+        r = reps[i % replicas]
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        for k in host_idx:
+            dev_idx[k].copy_(host_idx[k], non_blocking=True)
+        if n_pairs:
+            B.pa_copy_blocks(r["k_pool"], r["v_pool"], dev_idx["pairs"], err_word=err)
+        B.pa_reshape_and_cache(dev_in["k_new"], dev_in["v_new"], r["k_pool"], r["v_pool"],
+                               dev_idx["sm"], err_word=err)
+        B.pa_decode(outs[i % replicas], dev_in["q"], r["k_pool"], r["v_pool"], dev_idx["bt"],
+                    dev_idx["sl"], wl.scale, max_seq_len=wl.max_seq_len,
+                    workspace=wss[i % replicas], partition_tokens=P, err_word=err)
+        host_out.copy_(outs[i % replicas], non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()  # the caller needs the result
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    w1 = time.perf_counter()
+    barrier()
+    e2e_s = w1 - w0
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = world * kv_bytes * e2e_steps / e2e_s / 1e9
+
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "decode_kernel (pa_decode)",
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "alg_bytes_per_launch": alg_bytes,
+                "decode_ms_avg": dec_avg_ms}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
+        seqs, tok = cpu_sample_seqs(wl, budget)
+        sub = W_make_values_subset(wl, seqs)
+        cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"])  # load + warm
+        c0 = time.perf_counter()
+        reps_cpu = 0
+        nbytes = 0
+        while True:
+            nbytes += cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"])
+            reps_cpu += 1
+            if time.perf_counter() - c0 > 10.0 or reps_cpu >= 50:
+                break
+        cdt = time.perf_counter() - c0
+        cpu = {"value": nbytes / cdt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(seqs)} of {wl.num_seqs} sequences ({tok} tokens, all "
+                         f"{wl.n_q_heads} query heads) x {reps_cpu} repetitions, "
+                         f"{cdt:.1f} s, single thread"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs,
+                   "tokens_attended": wl.tokens_attended, "n_q_heads": wl.n_q_heads,
+                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "partition_tokens": P_res,
+                   "cow_pairs": n_pairs, "kv_bytes_per_step": kv_bytes,
+                   "l2": f"inputs rotated over {replicas} replicas "
+                         f"({replicas * kv_bytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2)",
+                   "arithmetic": "bf16 operands, fp32 accumulation and softmax",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_attended_per_s": tokens_per_s,
+        "pct_of_peak": 100.0 * value / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "note": "pinned host inputs copied in, result copied out and synchronised "
+                        "every step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

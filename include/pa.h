@@ -1,0 +1,207 @@
+/*
+ * pa.h — C ABI of the paged KV-cache decode library (libpa.so, sm_103a).
+ *
+ * The hot path of one decode step over a paged KV cache, as three calls:
+ *   pa_copy_blocks        copy-on-write block duplication
+ *   pa_reshape_and_cache  write each new token's K/V into its slot
+ *   pa_decode             attention of one query per sequence over its
+ *                         cached K/V, gathered through the block table
+ * A step issues them in that order on one stream: copy, then write, then
+ * attend (the new token attends to itself).
+ *
+ * Sources (web pages on PagedAttention):
+ *   "03 · PagedAttention" (sunilkunchoor.github.io): "Blocks and block
+ *     tables", "The part the analogy hides: the kernel", "Sharing:
+ *     copy-on-write, straight from fork()".
+ *   "PagedAttention" (mlapandio.dev daily terms): definition, the pool and
+ *     block-table diagram, "A DECODE STEP" and "COPY-ON-WRITE ON A SHARED
+ *     PREFIX" diagrams.
+ *   "Serving: vLLM and PagedAttention" (henryfzh-note.com), section 2.2
+ *     "Paging: the block table as virtual memory".
+ *
+ * Data layout (the pages fix only that a block holds block_size consecutive
+ * tokens and is reached through a per-sequence table; the rest is this
+ * library's convention):
+ *   k_pool, v_pool  bf16 [num_blocks][n_kv_heads][block_size][head_dim]:
+ *                   one (block, kv head) is a contiguous block_size*head_dim
+ *                   run of bf16 (4 KiB at block 16, head_dim 128).
+ *   block_tables    int32 [num_seqs][max_blocks_per_seq], row-major; entry j
+ *                   of row s is the physical block of tokens
+ *                   [j*block_size, (j+1)*block_size) of sequence s.
+ *   seq_lens        int32 [num_seqs]: tokens to attend, new token included.
+ *   q, out          bf16 [num_seqs][n_q_heads][head_dim].
+ *   slot            physical_block * block_size + (position mod block_size).
+ *   GQA             query head h reads kv head h / (n_q_heads / n_kv_heads).
+ *
+ * Ownership and execution: every pointer argument is DEVICE memory owned by
+ * the caller (unless stated otherwise); the library keeps no device
+ * allocation of its own. Every call is asynchronous on `stream` (0 = legacy
+ * default stream) and returns after enqueueing. The return status covers
+ * host-side argument checks and launch errors only. Problems only the device
+ * can see (a block id or slot outside the pool, a length beyond the table)
+ * never trap: the offending access is skipped and a bit is OR-ed into
+ * *err_word (a device int32 the caller zeroes and reads; NULL = do not
+ * report). Bad data never makes a kernel read or write outside the buffers
+ * described by the arguments.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer,
+                             n_q_heads % n_kv_heads != 0, workspace too small */
+  PA_ERR_UNSUPPORTED = 2, /* head_dim not 64/128, block_size not 8/16/32,
+                             n_q_heads / n_kv_heads > 16, partition size */
+  PA_ERR_CUDA = 3         /* a CUDA runtime/driver call failed; see
+                             pa_last_cuda_error() */
+} pa_status;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define PA_DEV_ERR_BLOCK_ID 0x1 /* table entry outside [0, num_blocks): its
+                                   tokens are treated as absent */
+#define PA_DEV_ERR_SLOT 0x2     /* slot >= num_blocks*block_size: not written */
+#define PA_DEV_ERR_PAIR 0x4     /* copy pair id outside the pool: skipped */
+#define PA_DEV_ERR_SEQ_LEN 0x8  /* seq_len < 0, > max_blocks_per_seq*block_size
+                                   or > max_seq_len: clamped into range */
+#define PA_DEV_ERR_TIMEOUT 0x10 /* a bounded wait inside a kernel gave up; the
+                                   output is undefined and the workspace must
+                                   be zeroed again before the next pa_decode */
+
+/* Human-readable name of a status. Never NULL. */
+const char* pa_status_string(pa_status s);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+   ("" if none). Valid until the next call on that thread. */
+const char* pa_last_cuda_error(void);
+
+/*
+ * Partition size pa_decode uses, in tokens: `partition_tokens` itself when
+ * non-zero (checked: a multiple of max(16, block_size), at most
+ * 128*max(16, block_size)), else the library's automatic choice, a pure
+ * function of the arguments. Returns a negative value for unsupported
+ * arguments.
+ */
+int pa_decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int max_seq_len,
+                               int partition_tokens);
+
+/*
+ * Bytes of device workspace pa_decode needs for these arguments (same
+ * meaning as in pa_decode). The workspace holds the split-KV partial
+ * results and a few counters. It must be ZEROED before its first use
+ * (cudaMemset / torch.zeros); pa_decode leaves it zeroed again when it
+ * completes, so one workspace can serve any number of stream-ordered
+ * calls. Calls that may run concurrently need separate workspaces.
+ * Returns 0 for unsupported arguments.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int block_size, int max_seq_len, int partition_tokens);
+
+/*
+ * pa_decode — paged decode attention.
+ * Defined by "03 · PagedAttention", "The part the analogy hides: the
+ * kernel" (the kernel takes the block table and gathers K/V from scattered
+ * blocks during attention) and the "A DECODE STEP" diagram of
+ * "PagedAttention" (mlapandio.dev: one launch for the whole batch; each
+ * sequence's query is scored against every key in its blocks).
+ *
+ * For every sequence s and query head h (kv head g = h / G,
+ * G = n_q_heads / n_kv_heads), with K_i, V_i the rows of token i < len_s
+ * gathered as k_pool[block_tables[s][i / block_size]][g][i % block_size]:
+ *   out[s][h] = sum_i softmax_i(scale * <q[s][h], K_i>) * V_i
+ * in fp32 arithmetic on bf16 inputs, rounded to bf16 (nearest even).
+ * A sequence with len_s == 0 gets zeros.
+ *
+ * Each sequence's tokens are split into partitions of
+ * pa_decode_partition_tokens(...) tokens; partitions are processed in
+ * parallel and their partial results merged with a log-sum-exp reduction
+ * (the same value as unsplit attention, up to fp32 rounding).
+ *
+ *   out                bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
+ *   q                  bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
+ *   k_pool, v_pool     bf16 [num_blocks][n_kv_heads][block_size][head_dim],
+ *                      16-B aligned
+ *   block_tables       int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                      ceil(len_s / block_size) entries of row s are read
+ *   seq_lens           int32 [num_seqs]
+ *   num_seqs           >= 0 (0: nothing is launched), <= 65536
+ *   max_blocks_per_seq >= 1 (row stride of block_tables)
+ *   num_blocks         >= 1, num_blocks*n_kv_heads*block_size < 2^31
+ *   n_q_heads, n_kv_heads  >= 1, n_q_heads % n_kv_heads == 0, G <= 16
+ *   head_dim           64 or 128
+ *   block_size         8, 16 or 32
+ *   scale              softmax scale (e.g. 1/sqrt(head_dim))
+ *   partition_tokens   0 = automatic, else see pa_decode_partition_tokens
+ *   max_seq_len        host-side upper bound of seq_lens (sizes the
+ *                      workspace); longer sequences are clamped and flagged
+ *   workspace          >= pa_decode_workspace_bytes(...) bytes, 256-B
+ *                      aligned, zeroed before first use (see above)
+ *   err_word           nullable device int32, see PA_DEV_ERR_*
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                    int max_blocks_per_seq, int num_blocks, int n_q_heads, int n_kv_heads,
+                    int head_dim, int block_size, float scale, int partition_tokens,
+                    int max_seq_len, void* workspace, size_t workspace_bytes,
+                    int32_t* err_word, pa_stream_t stream);
+
+/*
+ * pa_reshape_and_cache — write new tokens' K/V into their pool slots.
+ * Defined by the "A DECODE STEP" diagram of "PagedAttention"
+ * (mlapandio.dev): the step writes the new K and V into the sequence's
+ * current block; "03 · PagedAttention", "Blocks and block tables": that
+ * block was taken when the previous one filled.
+ *
+ * For token t with slot = slot_mapping[t] >= 0, every kv head h:
+ *   k_pool[slot / block_size][h][slot % block_size][:] = k[t][h][:]
+ *   v_pool[slot / block_size][h][slot % block_size][:] = v[t][h][:]
+ * (bit copy). slot < 0 is padding and is skipped silently; slot >=
+ * num_blocks*block_size is skipped and flagged PA_DEV_ERR_SLOT. Two tokens
+ * naming the same slot race (the caller must not do that).
+ *
+ *   k, v          bf16 [num_tokens][n_kv_heads][head_dim], 16-B aligned
+ *   k_pool, v_pool as in pa_decode
+ *   slot_mapping  int32 [num_tokens]
+ *   num_tokens    >= 0 (0: nothing is launched)
+ */
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                               const int32_t* slot_mapping, int num_tokens, int num_blocks,
+                               int n_kv_heads, int head_dim, int block_size,
+                               int32_t* err_word, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks — copy-on-write block duplication.
+ * Defined by "03 · PagedAttention", "Sharing: copy-on-write, straight from
+ * fork()" (a writer into a block with refcount > 1 gets a copy and its
+ * table is repointed) and the "COPY-ON-WRITE ON A SHARED PREFIX" diagram of
+ * "PagedAttention" (mlapandio.dev: the runtime copies the shared block,
+ * then writes). The refcount bookkeeping and the table update are the
+ * caller's (host) business; this call moves the bytes.
+ *
+ * For each pair p: block pairs[p][1] of k_pool and of v_pool (all kv heads)
+ * becomes a bit copy of block pairs[p][0]. A pair with an id outside
+ * [0, num_blocks) is skipped and flagged PA_DEV_ERR_PAIR. Precondition: no
+ * destination id is also a source id or appears twice (else the result
+ * depends on scheduling).
+ *
+ *   pairs    int32 [n_pairs][2] (src, dst), device memory
+ *   n_pairs  >= 0 (0: nothing is launched)
+ */
+pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs,
+                         int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                         int32_t* err_word, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,188 @@
+"""Thin ctypes binding of ``libpa.so`` (declared in ``include/pa.h``).
+
+Argument marshalling only: tensors are checked for dtype, device, shape and
+contiguity, their sizes and data pointers are passed through, and a
+non-zero status becomes an exception. Every step of the computation runs
+in the library's CUDA kernels; there is no fallback. If the library has not
+been built, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_DEV_ERR_BLOCK_ID = 0x1
+PA_DEV_ERR_SLOT = 0x2
+PA_DEV_ERR_PAIR = 0x4
+PA_DEV_ERR_SEQ_LEN = 0x8
+PA_DEV_ERR_TIMEOUT = 0x10
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = C.c_void_p
+_i = C.c_int
+
+SIGNATURES = {
+    "pa_status_string": (C.c_char_p, [_i]),
+    "pa_last_cuda_error": (C.c_char_p, []),
+    "pa_decode_partition_tokens": (_i, [_i, _i, _i, _i, _i]),
+    "pa_decode_workspace_bytes": (C.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
+    "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
+                       _i, _i, _vp, C.c_size_t, _vp, _vp]),
+    "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "pa_copy_blocks": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+}
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn, status):
+        L = lib()
+        name = L.pa_status_string(status).decode()
+        detail = L.pa_last_cuda_error().decode() if status == PA_ERR_CUDA else ""
+        super().__init__(f"{fn}: {name}" + (f" ({detail})" if detail else ""))
+        self.status = status
+
+
+def lib():
+    """The loaded ``libpa.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(
+                    f"{_build.LIB} is missing: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = C.CDLL(_build.LIB)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(t, name, dtype, dim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got {tuple(t.shape)}")
+
+
+def pa_decode_partition_tokens(num_seqs, n_kv_heads, block_size, max_seq_len,
+                               partition_tokens=0) -> int:
+    r = lib().pa_decode_partition_tokens(num_seqs, n_kv_heads, block_size, max_seq_len,
+                                         partition_tokens)
+    if r < 0:
+        raise ValueError("unsupported decode arguments")
+    return r
+
+
+def pa_decode_workspace_bytes(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                              max_seq_len, partition_tokens=0) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, n_q_heads, n_kv_heads, head_dim,
+                                               block_size, max_seq_len, partition_tokens))
+
+
+def decode_workspace(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_seq_len,
+                     partition_tokens=0, device=None) -> torch.Tensor:
+    """A zeroed workspace for pa_decode (it stays zeroed between calls)."""
+    n = pa_decode_workspace_bytes(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                  max_seq_len, partition_tokens)
+    if n == 0:
+        raise ValueError("unsupported decode arguments")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale, *, max_seq_len,
+              workspace, partition_tokens=0, err_word=None, stream=None):
+    """out[s, h] = softmax(scale * q[s, h] . K) V over the tokens of sequence s,
+    K/V gathered from k_pool/v_pool through block_tables (see include/pa.h)."""
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _check(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _check(block_tables, "block_tables", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _check(workspace, "workspace", torch.uint8, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    if tuple(out.shape) != (S, Hq, D) or D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens must have one row per sequence")
+    st = lib().pa_decode(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                         _ptr(seq_lens), S, block_tables.shape[1], NB, Hq, Hkv, D, bs,
+                         float(scale), int(partition_tokens), int(max_seq_len),
+                         _ptr(workspace), workspace.numel(), _ptr(err_word),
+                         _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_decode", st)
+    return out
+
+
+def pa_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, *, err_word=None, stream=None):
+    """k_pool[slot // bs, :, slot % bs] = k[t] (and v) for every slot >= 0."""
+    dev = k.device
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _check(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _check(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    T, Hkv, D = k.shape
+    NB, Hkv2, bs, D2 = k_pool.shape
+    if v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch between new K/V and the pools")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    st = lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool),
+                                    _ptr(slot_mapping), T, NB, Hkv, D, bs, _ptr(err_word),
+                                    _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_reshape_and_cache", st)
+
+
+def pa_copy_blocks(k_pool, v_pool, pairs, *, err_word=None, stream=None):
+    """Block pairs[p, 1] of both pools becomes a copy of block pairs[p, 0]."""
+    dev = k_pool.device
+    _check(k_pool, "k_pool", torch.bfloat16, 4)
+    _check(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _check(pairs, "pairs", torch.int32, 2, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    NB, Hkv, bs, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or (pairs.numel() and pairs.shape[1] != 2):
+        raise ValueError("pools must match and pairs must be [n, 2]")
+    st = lib().pa_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), pairs.shape[0], Hkv, D,
+                              bs, NB, _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_copy_blocks", st)

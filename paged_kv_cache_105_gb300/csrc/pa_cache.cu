@@ -1,0 +1,127 @@
+// Cache writes of one decode step: the new tokens' K/V into their slots, and
+// copy-on-write block duplication. Both are bit copies in 16-byte vectors;
+// a (block, kv head) run and a token's head row are contiguous, so every
+// warp reads and writes whole 128-byte lines.
+//
+// Sources: "PagedAttention" (mlapandio.dev), "A DECODE STEP" diagram (the
+// step writes the new K and V into the current block) and "COPY-ON-WRITE ON
+// A SHARED PREFIX" diagram (copy the shared block, then write);
+// "03 · PagedAttention", "Sharing: copy-on-write, straight from fork()".
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+// One thread per 16-byte chunk of one (token, kv head) row of K or V.
+__global__ void __launch_bounds__(256)
+reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                         uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                         const int32_t* __restrict__ slot_mapping, int num_tokens,
+                         int num_blocks, int n_kv, int chunks_per_row, int block_size,
+                         int32_t* err) {
+  const int64_t per_tensor = (int64_t)num_tokens * n_kv * chunks_per_row;
+  const int64_t total = 2 * per_tensor;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per_tensor;
+    const int64_t r = is_v ? i - per_tensor : i;
+    const int c = (int)(r % chunks_per_row);
+    const int64_t th = r / chunks_per_row;  // token * n_kv + head
+    const int h = (int)(th % n_kv);
+    const int t = (int)(th / n_kv);
+    const int32_t slot = __ldg(&slot_mapping[t]);
+    if (slot < 0) continue;  // padding
+    if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
+      if (c == 0 && h == 0 && !is_v) report(err, PA_DEV_ERR_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    const int64_t dst = ((blk * n_kv + h) * block_size + off) * chunks_per_row + c;
+    const int64_t src = th * chunks_per_row + c;
+    if (is_v)
+      v_pool[dst] = __ldg(&v[src]);
+    else
+      k_pool[dst] = __ldg(&k[src]);
+  }
+}
+
+// grid.y = pair; threads stride over the 16-byte chunks of one block of K
+// followed by the same block of V.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                   const int32_t* __restrict__ pairs, int num_blocks, int64_t chunks_per_block,
+                   int32_t* err) {
+  const int p = blockIdx.y;
+  const int32_t src = __ldg(&pairs[2 * p]);
+  const int32_t dst = __ldg(&pairs[2 * p + 1]);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(err, PA_DEV_ERR_PAIR);
+    return;
+  }
+  const int64_t total = 2 * chunks_per_block;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= chunks_per_block;
+    const int64_t c = is_v ? i - chunks_per_block : i;
+    uint4* pool = is_v ? v_pool : k_pool;
+    pool[(int64_t)dst * chunks_per_block + c] = pool[(int64_t)src * chunks_per_block + c];
+  }
+}
+
+static bool supported_dims(int head_dim, int block_size) {
+  return (head_dim == 64 || head_dim == 128) &&
+         (block_size == 8 || block_size == 16 || block_size == 32);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_pool,
+                                          void* v_pool, const int32_t* slot_mapping,
+                                          int num_tokens, int num_blocks, int n_kv_heads,
+                                          int head_dim, int block_size, int32_t* err_word,
+                                          pa_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || n_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (!supported_dims(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_blocks * n_kv_heads * block_size >= (int64_t)1 << 31)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_pool || !v_pool || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PA_ERR_INVALID_ARG;
+  const int chunks = head_dim * 2 / 16;
+  const int64_t total = 2LL * num_tokens * n_kv_heads * chunks;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+      (const uint4*)k, (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping,
+      num_tokens, num_blocks, n_kv_heads, chunks, block_size, err_word);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_reshape_and_cache launch", e);
+}
+
+extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs,
+                                    int n_pairs, int n_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, int32_t* err_word, pa_stream_t stream) {
+  if (n_pairs < 0 || num_blocks <= 0 || n_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (!supported_dims(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (n_pairs > 65535) return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!k_pool || !v_pool || !pairs) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_INVALID_ARG;
+  const int64_t chunks = (int64_t)n_kv_heads * block_size * head_dim * 2 / 16;
+  const int threads = 256;
+  int64_t bx = (2 * chunks + threads - 1) / threads;
+  if (bx > 64) bx = 64;
+  dim3 grid((unsigned)bx, (unsigned)n_pairs);
+  copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
+      (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks launch", e);
+}

@@ -1,0 +1,122 @@
+"""Shared test plumbing: run one decode step through the C ABI, and compute
+the oracle's answer from the generator's inputs (never from GPU output)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import paref
+from paged_kv_cache_105_gb300 import binding as B
+from paged_kv_cache_105_gb300 import workloads as W
+
+ATOL = 1e-2       # max abs error, bf16 output vs fp64 oracle
+ROW_RTOL = 2e-2   # max over (seq, head) rows of ||gpu - ref||_2 / ||ref||_2
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor (any device) -> uint16 numpy array of its bit patterns."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_dev(wl: W.Workload, device):
+    d = dict(
+        block_tables=torch.from_numpy(wl.block_tables).to(device),
+        seq_lens=torch.from_numpy(wl.seq_lens).to(device),
+        slot_mapping=torch.from_numpy(wl.slot_mapping).to(device),
+        pairs=torch.from_numpy(np.ascontiguousarray(wl.cow_pairs.reshape(-1, 2))).to(device),
+    )
+    return d
+
+
+def gpu_step(wl: W.Workload, vals: dict, partition_tokens=None, workspace=None, err=None,
+             run_writes=True, max_seq_len=None):
+    """copy_blocks -> reshape_and_cache -> decode on the tensors in `vals`
+    (modified in place). Returns (out, err_word value)."""
+    dev = vals["q"].device
+    t = to_dev(wl, dev)
+    P = wl.partition_tokens if partition_tokens is None else partition_tokens
+    msl = wl.max_seq_len if max_seq_len is None else max_seq_len
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                                       wl.block_size, msl, P, device=dev)
+    out = torch.full_like(vals["q"], float("nan"))
+    if run_writes:
+        B.pa_copy_blocks(vals["k_pool"], vals["v_pool"], t["pairs"], err_word=err)
+        B.pa_reshape_and_cache(vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"],
+                               t["slot_mapping"], err_word=err)
+    B.pa_decode(out, vals["q"], vals["k_pool"], vals["v_pool"], t["block_tables"],
+                t["seq_lens"], wl.scale, max_seq_len=msl, workspace=workspace,
+                partition_tokens=P, err_word=err)
+    torch.cuda.synchronize()
+    return out, int(err.item())
+
+
+def oracle_step(wl: W.Workload, vals_cpu: dict):
+    """The oracle's copy -> write -> attention on host copies of the inputs.
+    Returns (out fp64 [S,Hq,d], k_pool bits, v_pool bits)."""
+    kp, vp = bits(vals_cpu["k_pool"]).copy(), bits(vals_cpu["v_pool"]).copy()
+    paref.copy_blocks(kp, vp, wl.cow_pairs)
+    paref.reshape_and_cache(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
+                            wl.slot_mapping)
+    out = paref.attention_paged(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
+                                wl.scale)
+    return out, kp, vp
+
+
+def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs):
+    """Oracle rows for the sequences `seqs` of a workload too large to copy
+    whole: gather (before the GPU step touches the pool) only the blocks
+    those sequences read, plus their copy-on-write sources, into a compact
+    host pool, remap ids, and run the oracle's step there.
+    Returns out fp64 [len(seqs), Hq, d]."""
+    bs = wl.block_size
+    seqs = list(seqs)
+    pair_src = {int(dst): int(src) for src, dst in wl.cow_pairs}
+    need = []
+    for s in seqs:
+        nb = -(-int(wl.seq_lens[s]) // bs)
+        for b in wl.block_tables[s, :nb]:
+            need.append(int(b))
+            if int(b) in pair_src:
+                need.append(pair_src[int(b)])
+    ids = list(dict.fromkeys(need))
+    remap = {b: i for i, b in enumerate(ids)}
+    idx = torch.tensor(ids, dtype=torch.long, device=vals_dev["k_pool"].device)
+    kp = bits(vals_dev["k_pool"].index_select(0, idx)).copy()
+    vp = bits(vals_dev["v_pool"].index_select(0, idx)).copy()
+    maxb = wl.block_tables.shape[1]
+    bt = np.full((len(seqs), maxb), -1, np.int32)
+    slots, pairs = [], []
+    for i, s in enumerate(seqs):
+        nb = -(-int(wl.seq_lens[s]) // bs)
+        bt[i, :nb] = [remap[int(b)] for b in wl.block_tables[s, :nb]]
+        sl = int(wl.slot_mapping[s])
+        slots.append(-1 if sl < 0 else remap[sl // bs] * bs + sl % bs)
+        last = int(wl.block_tables[s, (int(wl.seq_lens[s]) - 1) // bs]) if nb else -1
+        if last in pair_src:
+            pairs.append((remap[pair_src[last]], remap[last]))
+    sel = torch.tensor(seqs, dtype=torch.long, device=vals_dev["q"].device)
+    q = bits(vals_dev["q"].index_select(0, sel))
+    kn = bits(vals_dev["k_new"].index_select(0, sel))
+    vn = bits(vals_dev["v_new"].index_select(0, sel))
+    paref.copy_blocks(kp, vp, np.array(pairs, np.int32).reshape(-1, 2))
+    paref.reshape_and_cache(kn, vn, kp, vp, np.array(slots, np.int32))
+    return paref.attention_paged(q, kp, vp, bt, wl.seq_lens[seqs].astype(np.int32), wl.scale)
+
+
+def compare(gpu_out: torch.Tensor, ref: np.ndarray, what=""):
+    """bf16 GPU output vs fp64 oracle: elementwise abs and row-wise relative."""
+    g = gpu_out.detach().float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    num = np.sqrt((err ** 2).sum(-1))
+    den = np.sqrt((ref ** 2).sum(-1))
+    rel = np.where(den > 0, num / np.maximum(den, 1e-30), num)
+    max_rel = float(rel.max()) if rel.size else 0.0
+    assert max_abs <= ATOL, f"{what}: max abs err {max_abs:.3e} > {ATOL}"
+    assert max_rel <= ROW_RTOL, f"{what}: max row rel err {max_rel:.3e} > {ROW_RTOL}"
+    return max_abs, max_rel

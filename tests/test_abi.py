@@ -1,0 +1,122 @@
+"""The C-ABI library loads, exports every function include/pa.h declares,
+and rejects bad arguments on the host (no GPU needed for any of this)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_105_gb300 import binding as B
+from paged_kv_cache_105_gb300 import build as _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s+\**\s*(pa_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("pa_decode", "pa_reshape_and_cache", "pa_copy_blocks",
+               "pa_decode_workspace_bytes", "pa_decode_partition_tokens",
+               "pa_status_string", "pa_last_cuda_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(B.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(L):
+    assert L.pa_status_string(0) == b"PA_OK"
+    assert L.pa_status_string(1) == b"PA_ERR_INVALID_ARG"
+    assert L.pa_status_string(2) == b"PA_ERR_UNSUPPORTED"
+    assert L.pa_status_string(3) == b"PA_ERR_CUDA"
+
+
+def test_partition_choice(L):
+    f = L.pa_decode_partition_tokens
+    assert f(16, 8, 16, 32768, 512) == 512
+    assert f(16, 8, 16, 32768, 100) < 0          # not a multiple of 16
+    assert f(16, 8, 32, 32768, 48) < 0           # not a multiple of the 32-token unit
+    assert f(16, 8, 16, 32768, 128 * 16 + 16) < 0
+    assert f(1, 1, 7, 10, 0) < 0                 # unsupported block size
+    for args in [(256, 32, 16, 4096), (64, 8, 16, 2048), (5, 8, 16, 1900), (1, 1, 8, 1)]:
+        P = f(*args, 0)
+        st = max(16, args[2])
+        assert P >= st and P % st == 0 and P <= 512
+
+
+def test_workspace_bytes(L):
+    f = L.pa_decode_workspace_bytes
+    n = f(16, 64, 8, 128, 16, 32768, 512)
+    parts = 32768 // 512
+    assert n >= 16 * 64 * parts * (128 * 4 + 8) + 16 * 8 * 4
+    assert f(16, 64, 8, 96, 16, 32768, 512) == 0      # head_dim 96 unsupported
+    assert f(16, 64, 7, 128, 16, 32768, 512) == 0     # heads not divisible
+    assert f(16, 64, 2, 128, 16, 32768, 512) == 0     # group of 32 > 16
+    assert f(1, 1, 1, 64, 16, 10**6, 64) == 0         # more than 1024 partitions
+
+
+# The two tests below pass fake addresses that host validation must reject
+# before any launch. They run only where no GPU is present, so that a
+# validation bug can never turn into a launch with those addresses.
+no_gpu = pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                            reason="host-validation tests use fake device addresses")
+
+
+def _decode(L, **kw):
+    args = dict(out=1 << 12, q=1 << 12, k=1 << 12, v=1 << 12, bt=1 << 12, sl=1 << 12, S=2,
+                maxb=4, NB=8, Hq=8, Hkv=2, D=128, bs=16, scale=0.1, P=0, maxlen=64,
+                ws=1 << 16, wsb=1 << 20, err=None, stream=None)
+    args.update(kw)
+    a = args
+    return L.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["sl"], a["S"], a["maxb"],
+                       a["NB"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["scale"], a["P"],
+                       a["maxlen"], a["ws"], a["wsb"], a["err"], a["stream"])
+
+
+@no_gpu
+def test_decode_host_validation(L):
+    INV, UNS = B.PA_ERR_INVALID_ARG, B.PA_ERR_UNSUPPORTED
+    assert _decode(L, q=None) == INV
+    assert _decode(L, ws=None) == INV
+    assert _decode(L, Hq=6, Hkv=4) == INV            # heads not divisible
+    assert _decode(L, D=96) == UNS
+    assert _decode(L, bs=12) == UNS
+    assert _decode(L, Hq=34, Hkv=2) == UNS           # group of 17
+    assert _decode(L, P=24) == UNS
+    assert _decode(L, maxlen=65) == INV              # beyond 4 blocks of 16
+    assert _decode(L, wsb=16) == INV                 # workspace too small
+    assert _decode(L, q=(1 << 12) + 2) == INV        # misaligned
+    assert _decode(L, ws=(1 << 16) + 16) == INV      # workspace not 256-B aligned
+    assert _decode(L, S=-1) == INV
+    assert _decode(L, S=0, q=None) == B.PA_OK        # nothing to do, no launch
+
+
+@no_gpu
+def test_cache_calls_host_validation(L):
+    INV, UNS = B.PA_ERR_INVALID_ARG, B.PA_ERR_UNSUPPORTED
+    p = 1 << 12
+    assert L.pa_reshape_and_cache(None, p, p, p, p, 4, 8, 2, 128, 16, None, None) == INV
+    assert L.pa_reshape_and_cache(p, p, p, p, p, 4, 8, 2, 80, 16, None, None) == UNS
+    assert L.pa_reshape_and_cache(p, p, p, p, p, -1, 8, 2, 128, 16, None, None) == INV
+    assert L.pa_reshape_and_cache(p + 8, p, p, p, p, 4, 8, 2, 128, 16, None, None) == INV
+    assert L.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 2, 128, 16, None,
+                                  None) == B.PA_OK
+    assert L.pa_copy_blocks(None, p, p, 3, 2, 128, 16, 8, None, None) == INV
+    assert L.pa_copy_blocks(p, p, p, 3, 2, 128, 4, 8, None, None) == UNS
+    assert L.pa_copy_blocks(p, p, p, -2, 2, 128, 16, 8, None, None) == INV
+    assert L.pa_copy_blocks(None, None, None, 0, 2, 128, 16, 8, None, None) == B.PA_OK

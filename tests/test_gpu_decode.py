@@ -1,0 +1,170 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Bar: every bf16 output within 1e-2 of the oracle, and every (sequence, head)
+row within 2e-2 relative L2 error. Small workloads are compared in full;
+the two large ones (the fragmented MHA sweep and the 32k-token split-KV
+batch) at their full sizes, on sampled sequences the oracle can afford."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_105_gb300 import binding as B
+from paged_kv_cache_105_gb300 import workloads as W
+from tests.helpers import bits, compare, gpu_step, oracle_step, sampled_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def on_dev(vals):
+    return {k: v.to(DEV) for k, v in vals.items()}
+
+
+def full_parity(wl, partition_tokens=None, poison=True):
+    vals_cpu = W.make_values(wl, poison_tails=poison)
+    ref, kp, vp = oracle_step(wl, vals_cpu)
+    vals = on_dev(vals_cpu)
+    out, err = gpu_step(wl, vals, partition_tokens=partition_tokens)
+    assert err == 0
+    assert np.array_equal(bits(vals["k_pool"]), kp)
+    assert np.array_equal(bits(vals["v_pool"]), vp)
+    return compare(out, ref, wl.name), out, ref
+
+
+def test_worked_example_config():
+    (a, r), _, _ = full_parity(W.config1())
+    assert a < 1e-2 and r < 2e-2
+
+
+def test_gqa_batch_config():
+    full_parity(W.config2())
+
+
+def test_prefix_sharing_config():
+    wl = W.config4()
+    assert len(wl.cow_pairs) > 100
+    full_parity(wl)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_fragmented_mha_full_size_sampled(bs):
+    wl = W.config3(block_size=bs)
+    vals = W.make_values(wl, device=DEV, poison_tails=True)
+    rng = np.random.default_rng(bs)
+    order = np.argsort(wl.seq_lens)
+    seqs = sorted(set([int(order[0]), int(order[-1])] +
+                      rng.choice(wl.num_seqs, 4, replace=False).tolist()))
+    ref = sampled_oracle(wl, vals, seqs)
+    out, err = gpu_step(wl, vals)
+    assert err == 0
+    compare(out[seqs], ref, wl.name)
+
+
+def test_long_context_full_size_sampled():
+    wl = W.config5()
+    vals = W.make_values(wl, device=DEV, poison_tails=True)
+    seqs = [0, 11]
+    ref = sampled_oracle(wl, vals, seqs)
+    out, err = gpu_step(wl, vals)
+    assert err == 0
+    compare(out[seqs], ref, wl.name)
+    # every other row is at least finite and a convex mix of values
+    assert torch.isfinite(out.float()).all()
+
+
+LEN_MIX = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256,
+           257, 511, 512, 513, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (8, 1), (32, 2)])
+def test_length_mix_all_shapes(d, bs, hq, hkv):
+    wl = W.custom(LEN_MIX, block_size=bs, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                  seed=d * 7 + bs * 3 + hq + hkv, name=f"mix-d{d}-bs{bs}-{hq}q{hkv}kv")
+    full_parity(wl)
+
+
+@pytest.mark.parametrize("P", [16, 32, 64, 128, 512, 2048])
+def test_partition_sizes_agree(P):
+    wl = W.custom([1, 40, 300, 777, 2049, 4000], block_size=16, n_q_heads=16, n_kv_heads=2,
+                  head_dim=128, seed=5)
+    full_parity(wl, partition_tokens=P)
+
+
+def test_empty_sequences_give_zeros():
+    wl = W.custom([0, 5, 0, 300, 0], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=64,
+                  seed=9)
+    (_, _), out, _ = full_parity(wl)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0) and torch.all(out[4] == 0)
+
+
+def test_single_token_returns_its_value():
+    wl = W.custom([1, 1, 1], block_size=16, n_q_heads=8, n_kv_heads=2, head_dim=128, seed=4)
+    vals_cpu = W.make_values(wl)
+    vals = on_dev(vals_cpu)
+    out, err = gpu_step(wl, vals)
+    assert err == 0
+    v_new = vals_cpu["v_new"]                                # the only token is the new one
+    want = v_new.repeat_interleave(4, dim=1)                 # q head h reads kv head h // 4
+    assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+
+
+def test_workspace_reuse_is_deterministic():
+    wl = W.custom([50, 3000, 7, 1200, 4096], block_size=16, n_q_heads=32, n_kv_heads=8,
+                  head_dim=128, seed=6)
+    vals = on_dev(W.make_values(wl))
+    ws = B.decode_workspace(wl.num_seqs, 32, 8, 128, 16, wl.max_seq_len, 128, device=DEV)
+    first, err = gpu_step(wl, vals, partition_tokens=128, workspace=ws)
+    assert err == 0
+    for _ in range(3):
+        again, err = gpu_step(wl, vals, partition_tokens=128, workspace=ws, run_writes=False)
+        assert err == 0
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+
+
+def test_block_placement_does_not_matter():
+    base = W.custom([900, 33, 1500], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128,
+                    seed=21)
+    vals = W.make_values(base)
+    ref, _, _ = oracle_step(base, vals)
+    out1, _ = gpu_step(base, on_dev(vals))
+    # the same tokens under another placement: move every block to a new id
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(base.num_blocks)
+    moved = W.Workload(**{**base.__dict__})
+    moved.block_tables = np.where(base.block_tables >= 0, perm[base.block_tables], -1).astype(
+        np.int32)
+    moved.slot_mapping = (perm[base.slot_mapping // 16] * 16 + base.slot_mapping % 16).astype(
+        np.int32)
+    inv = np.argsort(perm)
+    vals2 = dict(vals)
+    vals2["k_pool"] = vals["k_pool"][torch.from_numpy(inv)]
+    vals2["v_pool"] = vals["v_pool"][torch.from_numpy(inv)]
+    out2, _ = gpu_step(moved, on_dev(vals2))
+    compare(out2, ref, "moved")
+    compare(out1, ref, "base")
+
+
+def test_bad_block_id_is_flagged_and_skipped():
+    wl = W.custom([40, 40], block_size=16, n_q_heads=4, n_kv_heads=4, head_dim=64, seed=8)
+    vals_cpu = W.make_values(wl)
+    good_ref, _, _ = oracle_step(wl, vals_cpu)
+    bad = W.Workload(**{**wl.__dict__})
+    bad.block_tables = wl.block_tables.copy()
+    bad.block_tables[0, 1] = wl.num_blocks + 7        # outside the pool
+    out, err = gpu_step(bad, on_dev(vals_cpu))
+    assert err & B.PA_DEV_ERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    compare(out[1:], good_ref[1:], "untouched sequence")
+
+
+def test_length_beyond_hint_is_clamped_and_flagged():
+    wl = W.custom([100, 64], block_size=16, n_q_heads=4, n_kv_heads=4, head_dim=64, seed=10)
+    vals_cpu = W.make_values(wl)
+    out, err = gpu_step(wl, on_dev(vals_cpu), max_seq_len=80)
+    assert err & B.PA_DEV_ERR_SEQ_LEN
+    clamped = W.Workload(**{**wl.__dict__})
+    clamped.seq_lens = np.array([80, 64], np.int32)
+    ref, _, _ = oracle_step(clamped, vals_cpu)
+    compare(out, ref, "clamped")
