@@ -448,7 +448,7 @@ def main():
         while True:
             nbytes += cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"])
             reps_cpu += 1
-            if time.perf_counter() - c0 > 10.0 or reps_cpu >= 50:
+            if time.perf_counter() - c0 > 10.0 or reps_cpu >= 1000:
                 break
         cdt = time.perf_counter() - c0
         cpu = {"value": nbytes / cdt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
