@@ -200,6 +200,45 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n
                          int n_kv_heads, int head_dim, int block_size, int num_blocks,
                          int32_t* err_word, pa_stream_t stream);
 
+/*
+ * pa_decode_noalloc — pa_decode for callers that cannot allocate device
+ * memory. The paper has no counterpart; this is a library convenience.
+ *
+ * Some callers cannot obtain device memory at the point where they decode:
+ * a serving engine that hands all free HBM to its KV pool at start-up and
+ * allows no allocation afterwards, a plugin running inside a framework whose
+ * allocator owns the device, or latency-critical code that cannot afford an
+ * allocation call that may synchronise the device. They still own their
+ * inputs and outputs, but cannot provide pa_decode's workspace.
+ *
+ * This entry point computes exactly what pa_decode computes, with the same
+ * arguments minus the workspace. Its scratch is a fixed array of
+ * PA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device image: every
+ * GPU that loads the library holds those 64 MiB until the process exits. It
+ * calls no allocator (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ *  - The first call on a device looks the array's device address up (one
+ *    cudaGetSymbolAddress with that device current). Make that first call
+ *    before any stream capture.
+ *  - Each call first clears the scratch's counters on `stream` (an
+ *    asynchronous memset), then runs the decode on `stream`.
+ *  - All calls in the process share the one array. Calls that may overlap on
+ *    the GPU (different streams without ordering, or several host threads)
+ *    race on it and give wrong results; order them on one stream.
+ *  - If the call would need more scratch than PA_NOALLOC_SCRATCH_BYTES
+ *    (compare pa_decode_workspace_bytes with it beforehand), it returns
+ *    PA_ERR_INVALID_ARG without launching anything. Everything else returns
+ *    what pa_decode returns for the same arguments.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                            int max_blocks_per_seq, int num_blocks, int n_q_heads,
+                            int n_kv_heads, int head_dim, int block_size, float scale,
+                            int partition_tokens, int max_seq_len, int32_t* err_word,
+                            pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

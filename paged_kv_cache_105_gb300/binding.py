@@ -38,7 +38,12 @@ SIGNATURES = {
                        _i, _i, _vp, C.c_size_t, _vp, _vp]),
     "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "pa_copy_blocks": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "pa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                               C.c_float, _i, _i, _vp, _vp]),
 }
+
+# Size of the library's fixed scratch used by pa_decode_noalloc (64 MiB).
+PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class PAError(RuntimeError):
@@ -186,3 +191,40 @@ def pa_copy_blocks(k_pool, v_pool, pairs, *, err_word=None, stream=None):
                               bs, NB, _ptr(err_word), _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_copy_blocks", st)
+
+
+def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, *, max_seq_len,
+                      partition_tokens=0, err_word=None, stream=None):
+    """pa_decode without a workspace argument, for callers that cannot
+    allocate device memory where they decode (an engine that gave all free
+    HBM to its KV pool at start-up, a plugin whose host framework owns the
+    allocator, code that cannot afford an allocation that may synchronise the
+    device). Its scratch is the library's fixed 64 MiB device array, shared by
+    every call in the process: calls must not overlap on the GPU, and the
+    first call on a device should come before any stream capture."""
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _check(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _check(block_tables, "block_tables", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    if tuple(out.shape) != (S, Hq, D) or D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens must have one row per sequence")
+    need = pa_decode_workspace_bytes(S, Hq, Hkv, D, bs, int(max_seq_len), int(partition_tokens))
+    if need > PA_NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"pa_decode_noalloc: this batch needs {need} bytes of scratch, the "
+                         f"library's fixed scratch holds {PA_NOALLOC_SCRATCH_BYTES}")
+    st = lib().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                 _ptr(block_tables), _ptr(seq_lens), S, block_tables.shape[1],
+                                 NB, Hq, Hkv, D, bs, float(scale), int(partition_tokens),
+                                 int(max_seq_len), _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_decode_noalloc", st)
+    return out

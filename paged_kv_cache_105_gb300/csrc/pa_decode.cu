@@ -732,3 +732,81 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   if (head_dim == 64) return dispatch_bs<64>(block_size, a, k_pool, v_pool, items_upper, st);
   return dispatch_bs<128>(block_size, a, k_pool, v_pool, items_upper, st);
 }
+
+// ------------------------------------------------------------------ no-alloc
+
+namespace pa {
+
+// Scratch of pa_decode_noalloc: a fixed array in device memory that exists on
+// every GPU that loads this library, from module load until the process
+// exits. Host code must not use its name as an address; the device address is
+// looked up once per device below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call per device, with that device current). nullptr on failure.
+static void* noalloc_scratch(pa_status* st) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *st = cuda_fail("pa_decode_noalloc cudaGetDevice", e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) {
+    *st = cuda_fail_msg("pa_decode_noalloc", "device index above 63");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *st = cuda_fail("pa_decode_noalloc cudaGetSymbolAddress", e);
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* seq_lens, int num_seqs,
+                                       int max_blocks_per_seq, int num_blocks, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size,
+                                       float scale, int partition_tokens, int max_seq_len,
+                                       int32_t* err_word, pa_stream_t stream) {
+  const size_t need = pa_decode_workspace_bytes(num_seqs, n_q_heads, n_kv_heads, head_dim,
+                                                block_size, max_seq_len, partition_tokens);
+  if (need == 0 || num_seqs <= 0) {
+    // Unsupported arguments or nothing to do: pa_decode returns the status
+    // before it touches any memory.
+    return pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim,
+                     block_size, scale, partition_tokens, max_seq_len, nullptr, 0, err_word,
+                     stream);
+  }
+  if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_INVALID_ARG;
+  pa_status st = PA_OK;
+  void* scratch = noalloc_scratch(&st);
+  if (scratch == nullptr) return st;
+  // The tickets and work counters must start at zero. A completed call
+  // leaves them zeroed, but the array is shared by every call in the
+  // process, so clear them here rather than trust the previous caller.
+  const int P = resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len,
+                                  partition_tokens);
+  WsLayout w;
+  if (P <= 0 || !layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
+    return PA_ERR_UNSUPPORTED;
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.tick_off, 0,
+                                  w.total - w.tick_off, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("pa_decode_noalloc memset", e);
+  return pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                   max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim, block_size,
+                   scale, partition_tokens, max_seq_len, scratch, PA_NOALLOC_SCRATCH_BYTES,
+                   err_word, stream);
+}
