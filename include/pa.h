@@ -86,8 +86,8 @@ const char* pa_last_cuda_error(void);
 
 /*
  * Partition size pa_decode uses, in tokens: `partition_tokens` itself when
- * non-zero (checked: a multiple of max(16, block_size), at most
- * 128*max(16, block_size)), else the library's automatic choice, a pure
+ * non-zero (checked: a multiple of 16, at most 2048; a partition may start
+ * inside a 32-token block), else the library's automatic choice, a pure
  * function of the arguments. Returns a negative value for unsupported
  * arguments.
  */
@@ -124,7 +124,11 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  * Each sequence's tokens are split into partitions of
  * pa_decode_partition_tokens(...) tokens; partitions are processed in
  * parallel and their partial results merged with a log-sum-exp reduction
- * (the same value as unsplit attention, up to fp32 rounding).
+ * (the same value as unsplit attention, up to fp32 rounding). The call
+ * launches the decode kernel and, when some sequence may span more than one
+ * partition, a merge kernel after it. Both are programmatic dependent
+ * launches: they may start while the preceding kernel on the stream drains,
+ * and wait for it to complete before reading anything.
  *
  *   out                bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
  *   q                  bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
@@ -133,7 +137,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  *   block_tables       int32 [num_seqs][max_blocks_per_seq]; only the first
  *                      ceil(len_s / block_size) entries of row s are read
  *   seq_lens           int32 [num_seqs]
- *   num_seqs           >= 0 (0: nothing is launched), <= 65536
+ *   num_seqs           >= 0 (0: nothing is launched), <= 16384
  *   max_blocks_per_seq >= 1 (row stride of block_tables)
  *   num_blocks         >= 1, num_blocks*n_kv_heads*block_size < 2^31
  *   n_q_heads, n_kv_heads  >= 1, n_q_heads % n_kv_heads == 0, G <= 16

@@ -22,6 +22,7 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
                          const int32_t* __restrict__ slot_mapping, int num_tokens,
                          int num_blocks, int n_kv, int chunks_per_row, int block_size,
                          int32_t* err) {
+  griddep_launch_dependents();  // a dependent decode may start launching now
   const int64_t per_tensor = (int64_t)num_tokens * n_kv * chunks_per_row;
   const int64_t total = 2 * per_tensor;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

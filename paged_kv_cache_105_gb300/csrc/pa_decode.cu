@@ -8,24 +8,32 @@
 // below is this library's.
 //
 // Design (one GPU, HBM-bound: every step reads all cached K/V once):
-//  * Work items are (sequence, kv head, partition of P tokens). Items are
-//    numbered sequence-major from per-sequence prefix sums that every CTA
-//    builds in shared memory; persistent CTAs (a few per SM) take them from
-//    a global counter, so no CTA is launched for empty work.
-//  * A CTA has 4 warps. The item's 16-token units (a 16-token block, two
-//    8-token blocks, or one 32-token block) are dealt round-robin to the
-//    warps. Each warp runs its own STAGES-deep pipeline: one lane looks up
-//    the unit's physical block(s) and issues 2-D TMA tile loads of the K and
-//    V rows, 128-byte swizzled, completing on a per-stage mbarrier.
+//  * Work items are (sequence, kv head, partition of P tokens), numbered
+//    sequence-major from per-sequence prefix sums that every CTA builds in
+//    shared memory. Persistent CTAs (two per SM) take items from a global
+//    counter; a CTA learns its next-but-one item while it works on the
+//    current one, through a small shared-memory mailbox.
+//  * A CTA has 4 warps. An item's 16-token units are dealt round-robin to
+//    them and every warp streams its own units: lane 0 issues TMA tile loads
+//    (128-byte swizzle) of the unit's K and V rows into the warp's stage
+//    ring, one mbarrier per stage. Each warp keeps its ring full across item
+//    boundaries: the next item's table entries, query fragments and first
+//    units are already in flight while the CTA merges the current item.
 //  * The GQA group (the G query heads sharing the kv head) is the N side of
 //    bf16 mma.sync m16n8k16 with the tokens on M: S^T = K Q^T, then
-//    O^T += V^T P^T. movmatrix turns the score fragment into the P^T operand
-//    in registers. Online softmax in fp32 (base-2, running max per head).
-//  * Warps merge through shared memory; a one-partition sequence writes its
-//    bf16 output directly, otherwise the partition's (O, m, l) goes to the
-//    workspace and the last CTA to finish a (sequence, kv head) — decided by
-//    an atomic ticket, nobody waits — merges the partitions with
-//    log-sum-exp weights and writes the output.
+//    O^T += V^T P^T; movmatrix turns the score fragment into the P^T operand
+//    in registers. Online softmax in fp32, base 2.
+//  * Warps 1-3 hand their state to warp 0 through shared memory; a
+//    one-partition sequence writes its bf16 output directly, otherwise the
+//    partition's (O, m, l) goes to the workspace and a second, small kernel
+//    (one warp per query row) merges the partitions with log-sum-exp
+//    weights. It is a programmatic dependent launch: it starts while the
+//    decode grid drains and waits on the grid dependency before reading.
+//  * The decode grid itself is a programmatic dependent of whatever precedes
+//    it on the stream (normally the cache write), so its launch overlaps that
+//    kernel; it waits on the dependency before reading any input.
+//  * Every mbarrier wait is bounded; on timeout the kernel flags
+//    PA_DEV_ERR_TIMEOUT and keeps its control flow, so it always terminates.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -41,9 +49,12 @@ namespace pa {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a wait that long is a fault
+constexpr int kUnit = 16;                           // tokens per pipeline stage
+constexpr int kMaxUnitsPerPart = 128;               // lane-held table entries: 32 per warp
+constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s: a wait that long is a fault
+constexpr uint64_t kWaitAfterFaultNs = 1000000ull;  // 1 ms once something has timed out
 constexpr int kMaxParts = 1024;
-constexpr int kMaxSeqs = 65536;
+constexpr int kMaxSeqs = 16384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -53,33 +64,43 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   float* ws_o;               // [S][Hq][max_parts][D]  un-normalised partial outputs
   float2* ws_ml;             // [S][Hq][max_parts]     (running max, sum) in log2 units
-  int32_t* tickets;          // [S][Hkv]               partitions finished
-  int32_t* work;             // [2]: items handed out beyond the first wave, CTAs done
+  int32_t* work;             // [2]: items handed out dynamically, CTAs done
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
   int part_tokens, max_parts, len_cap;
+  int map3d;                 // 1: one TMA op loads both 64-column halves of a row
   float scale_log2;
 };
 
 template <int D, int BS, int NT>
 struct Cfg {
-  static constexpr int ST = BS < 16 ? 16 : BS;  // tokens per pipeline stage (one unit)
-  static constexpr int BPU = ST / BS;           // pool blocks per unit
-  static constexpr int KH = D / 64;             // 128-byte halves of a K/V row
-  static constexpr int TILE = ST * 128;         // bytes of one half of K or V for a unit
-  static constexpr int STAGE = 2 * KH * TILE;   // K + V bytes of a unit
-  static constexpr int STAGES_RAW = 24576 / STAGE;
+  static constexpr int ROWS = BS < kUnit ? BS : kUnit;  // rows per TMA box
+  static constexpr int BOXES = kUnit / ROWS;            // boxes (blocks) per unit
+  static constexpr int KH = D / 64;                     // 128-byte halves of a row
+  static constexpr int BOX_BYTES = KH * ROWS * 128;     // one box of K (or V), all halves
+  static constexpr int KV_BYTES = BOXES * BOX_BYTES;    // K (or V) of a unit = 16 * D * 2
+  static constexpr int STAGE = 2 * KV_BYTES;
+  static constexpr int BUDGET = NT == 1 ? 24576 : 16384;  // pipeline bytes per warp
+  static constexpr int STAGES_RAW = BUDGET / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
-  static constexpr int PIPE = kWarps * STAGES * STAGE;
-  static constexpr int MSTRIDE = D + 4;  // padded row of the cross-warp merge buffer
   static constexpr int HEADS = NT * 8;
-  static constexpr int MERGE = kWarps * HEADS * (MSTRIDE + 2) * 4;
-  static_assert(MERGE <= PIPE, "merge buffer must fit in the pipeline buffers");
-  static constexpr int BAR_OFF = PIPE;
-  static constexpr int MISC_OFF = BAR_OFF + kWarps * STAGES * 8;
-  static constexpr int PREFIX_OFF = MISC_OFF + 16;
-  static size_t smem_bytes(int num_seqs) {
-    return 1024 /* alignment slack */ + PREFIX_OFF + sizeof(int) * (size_t)(num_seqs + 1);
+  static constexpr int KS = D / 16;
+  static constexpr int MSTRIDE = D + 4;  // padded row of the merge buffer
+  static constexpr int PIPE_OFF = 0;
+  static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
+  static constexpr int NBARS = kWarps * STAGES + 4;  // stage barriers + mailbox
+  static constexpr int MAIL_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int MISC_OFF = MAIL_OFF + 16;
+  static constexpr int FIN_OFF = MISC_OFF + 16;      // 2 x 16 floats
+  static constexpr int ML_OFF = FIN_OFF + 2 * 16 * 4;  // 3 warps x HEADS x (m, l)
+  static constexpr int MERGE_OFF = ML_OFF + 3 * HEADS * 2 * 4;
+  // Merge buffer: 3 warps x G heads x MSTRIDE floats; then the prefix table.
+  __host__ __device__ static int prefix_off(int group) {
+    return MERGE_OFF + 3 * group * MSTRIDE * 4;
+  }
+  static size_t smem_bytes(int num_seqs, int group) {
+    return 1024 /* alignment slack */ + prefix_off(group) +
+           sizeof(int) * (size_t)(num_seqs + 1);
   }
 };
 
@@ -135,136 +156,238 @@ __device__ void build_prefix(int* prefix, const DecodeArgs& a, int* warp_tot) {
   if (tid == kThreads - 1) prefix[a.num_seqs] = base + incl;
 }
 
+// Bounded wait that flags a timeout (and shortens later waits) instead of
+// hanging; control flow continues either way.
+__device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, const DecodeArgs& a,
+                                             volatile int* fault) {
+  const uint64_t limit = *fault ? kWaitAfterFaultNs : kWaitLimitNs;
+  if (!mbar_wait_bounded(bar, parity, limit)) {
+    report(a.err, PA_DEV_ERR_TIMEOUT);
+    *fault = 1;
+  }
+}
+
+// What a warp needs to know about one item.
+struct Item {
+  int s, g, p, nparts, tok_end, u_begin, n_units;
+};
+
+__device__ __forceinline__ Item decode_item(int item, const int* prefix, const DecodeArgs& a) {
+  int lo = 0, hi = a.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.s = lo;
+  it.nparts = (prefix[lo + 1] - prefix[lo]) / a.n_kv;
+  const int local = item - prefix[lo];
+  it.g = local / it.nparts;
+  it.p = local - it.g * it.nparts;
+  const int len = clamp_len(__ldg(&a.seq_lens[lo]), a.len_cap);
+  const int tok_begin = it.p * a.part_tokens;
+  it.tok_end = min(len, tok_begin + a.part_tokens);
+  it.u_begin = tok_begin / kUnit;
+  it.n_units = it.tok_end > tok_begin ? (it.tok_end + kUnit - 1) / kUnit - it.u_begin : 0;
+  return it;
+}
+
+__device__ __forceinline__ int units_of_warp(const Item& it, int warp) {
+  return it.n_units > warp ? (it.n_units - warp + kWarps - 1) / kWarps : 0;
+}
+
+// Lane j gets the pool blocks of this warp's j-th unit of the item (one per
+// TMA box; -1 = outside the pool, -2 = no tokens there).
+template <int BS, int BOXES, int ROWS>
+__device__ __forceinline__ void load_ids(int (&ids)[BOXES], const Item& it, int warp, int lane,
+                                         const DecodeArgs& a) {
+  const int32_t* table = a.block_tables + (int64_t)it.s * a.max_blocks;
+  const int u = it.u_begin + warp + lane * kWarps;
+  const bool mine = lane < units_of_warp(it, warp);
+#pragma unroll
+  for (int b = 0; b < BOXES; ++b) {
+    ids[b] = -2;
+    const int tok = u * kUnit + b * ROWS;
+    if (mine && tok < it.tok_end) {
+      int id = __ldg(&table[tok / BS]);
+      if (id < 0 || id >= a.num_blocks) {
+        report(a.err, PA_DEV_ERR_BLOCK_ID);
+        id = -1;
+      }
+      ids[b] = id;
+    }
+  }
+}
+
+// B-operand fragments of the item's queries (head_dim x heads, column-major
+// = the q rows); heads past the group are zero.
+template <int D, int NT>
+__device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Item& it, int lane,
+                                       const DecodeArgs& a) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int n = t * 8 + (lane >> 2);
+    const bool real = n < a.group;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        a.q + ((int64_t)it.s * a.n_q + (int64_t)it.g * a.group + (real ? n : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qf[t][ks][0] = real ? __ldg(&qrow[ks * 8 + (lane & 3)]) : 0u;
+      qf[t][ks][1] = real ? __ldg(&qrow[ks * 8 + 4 + (lane & 3)]) : 0u;
+    }
+  }
+}
+
+#ifdef PA_TRACE
+// Per-CTA event log for timing studies: [cta][slot] = (event << 56) | ns.
+constexpr int kTraceSlots = 256;
+__device__ uint64_t g_trace[1024 * kTraceSlots];
+__device__ int g_trace_n[1024];
+#define PA_EVENT(ev)                                                              \
+  do {                                                                            \
+    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                  \
+      const int i_ = g_trace_n[blockIdx.x]++;                                     \
+      if (i_ < kTraceSlots)                                                       \
+        g_trace[blockIdx.x * kTraceSlots + i_] =                                  \
+            ((uint64_t)(ev) << 56) | (globaltimer_ns() & ((1ull << 56) - 1));     \
+    }                                                                             \
+  } while (0)
+#else
+#define PA_EVENT(ev) \
+  do {               \
+  } while (0)
+#endif
+
 template <int D, int BS, int NT>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
               const DecodeArgs a) {
   using C = Cfg<D, BS, NT>;
-  constexpr int ST = C::ST, BPU = C::BPU, KH = C::KH, STAGES = C::STAGES;
-  constexpr int KS = D / 16;  // 16-wide steps along head_dim
+  constexpr int ROWS = C::ROWS, BOXES = C::BOXES, KH = C::KH, STAGES = C::STAGES;
+  constexpr int KS = C::KS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t smem_base = smem_u32(smem);
-  const uint32_t bar_base = smem_base + C::BAR_OFF;
-  int* misc = reinterpret_cast<int*>(smem + C::MISC_OFF);  // [0] next item [1] last [2] abort
-  int* prefix = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
+  const uint32_t sbase = smem_u32(smem);
+  int* mail = reinterpret_cast<int*>(smem + C::MAIL_OFF);
+  int* misc = reinterpret_cast<int*>(smem + C::MISC_OFF);  // [1] fault flag
+  float* fin = reinterpret_cast<float*>(smem + C::FIN_OFF);
+  float* mlb = reinterpret_cast<float*>(smem + C::ML_OFF);
+  float* macc = reinterpret_cast<float*>(smem + C::MERGE_OFF);
+  int* prefix = reinterpret_cast<int*>(smem + C::prefix_off(a.group));
+  volatile int* fault = misc + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t my_pipe = sbase + C::PIPE_OFF + warp * STAGES * C::STAGE;
+  const uint32_t my_bar = sbase + C::BAR_OFF + warp * STAGES * 8;
+  const uint32_t mail_bar = sbase + C::BAR_OFF + kWarps * STAGES * 8;
 
   if (tid == 0) {
-    for (int i = 0; i < kWarps * STAGES; ++i) mbar_init(bar_base + 8 * i, 1);
-    misc[2] = 0;
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(sbase + C::BAR_OFF + 8 * i, 1);
+    misc[0] = 0;
+    misc[1] = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
-  {
-    // warp totals borrow the merge area (not yet in use)
-    int* warp_tot = reinterpret_cast<int*>(smem);
-    build_prefix(prefix, a, warp_tot);
-  }
+  griddep_wait();  // inputs may come from the previous kernel on the stream
+  build_prefix(prefix, a, reinterpret_cast<int*>(smem + C::ML_OFF));
   __syncthreads();
   const int total = prefix[a.num_seqs];
+  const int G = a.group;
+  PA_EVENT(1);
 
-  const uint32_t warp_pipe = smem_base + warp * STAGES * C::STAGE;
-  const uint32_t warp_bar = bar_base + warp * STAGES * 8;
-  uint32_t used = 0;  // stages this warp has consumed so far (same on all lanes)
+  // Items of this CTA: blockIdx.x, blockIdx.x + gridDim.x, then one per
+  // dynamic fetch (2 * gridDim.x + counter); the sequence only increases.
   int item = blockIdx.x;
-  uint32_t drain_from = 0, drain_to = 0;  // stages still in flight after a timeout
-
-  while (item < total) {
-    int next = 0;
-    if (tid == 0) next = atomicAdd(&a.work[0], 1) + (int)gridDim.x;
-
-    // ---- locate the item: sequence s, kv head g, partition p
-    int lo = 0, hi = a.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  Item cur{}, nxt{};
+  int ids_cur[BOXES], ids_nxt[BOXES];
+  uint32_t qf_cur[NT][KS][2], qf_nxt[NT][KS][2];
+  bool have_cur = item < total;
+  bool have_nxt = false;
+  if (have_cur) {
+    cur = decode_item(item, prefix, a);
+    load_ids<BS, BOXES, ROWS>(ids_cur, cur, warp, lane, a);
+    load_q<D, NT>(qf_cur, cur, lane, a);
+    const int item1 = item + (int)gridDim.x;
+    have_nxt = item1 < total;
+    if (have_nxt) {
+      nxt = decode_item(item1, prefix, a);
+      load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
+      load_q<D, NT>(qf_nxt, nxt, lane, a);
     }
-    const int s = lo;
-    const int nparts = (prefix[s + 1] - prefix[s]) / a.n_kv;
-    const int local = item - prefix[s];
-    const int g = local / nparts, p = local - g * nparts;
-    const int len = clamp_len(__ldg(&a.seq_lens[s]), a.len_cap);
-    const int tok_begin = p * a.part_tokens;
-    const int tok_end = min(len, tok_begin + a.part_tokens);
-    const int u_begin = tok_begin / ST;
-    const int n_units = tok_end > tok_begin ? (tok_end + ST - 1) / ST - u_begin : 0;
-    const int n_w = n_units > warp ? (n_units - warp + kWarps - 1) / kWarps : 0;
-    const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
+  }
 
-    // ---- lane k holds the physical block(s) of this warp's k-th unit
-    int ids[BPU];
-#pragma unroll
-    for (int b = 0; b < BPU; ++b) ids[b] = -2;  // -2: no tokens there
-    if (lane < n_w) {
-      const int u = u_begin + warp + lane * kWarps;
-#pragma unroll
-      for (int b = 0; b < BPU; ++b) {
-        const int j = u * BPU + b;
-        if (j * BS < tok_end) {
-          int id = __ldg(&table[j]);
-          if (id < 0 || id >= a.num_blocks) {
-            report(a.err, PA_DEV_ERR_BLOCK_ID);
-            id = -1;  // tokens of this block are treated as absent
-          }
-          ids[b] = id;
+  uint32_t issued = 0, consumed = 0;  // units of this warp (same on all lanes)
+  int issue_in_next = 0, issue_j = 0;  // issue cursor: (current or next item, unit)
+
+  // Issue TMA loads into free stages, running from the current item into the
+  // next one. Warp-collective.
+  auto fill = [&]() {
+#pragma unroll 1
+    while (issued - consumed < (uint32_t)STAGES) {
+      const int nm = issue_in_next ? units_of_warp(nxt, warp) : units_of_warp(cur, warp);
+      if (issue_j >= nm) {
+        if (!issue_in_next && have_nxt) {
+          issue_in_next = 1;
+          issue_j = 0;
+          continue;
         }
+        break;
       }
-    }
-
-    auto issue = [&](int k) {
-      int bid[BPU];
+      int bid[BOXES];
 #pragma unroll
-      for (int b = 0; b < BPU; ++b) bid[b] = __shfl_sync(0xffffffffu, ids[b], k);
+      for (int b = 0; b < BOXES; ++b)
+        bid[b] = __shfl_sync(0xffffffffu, issue_in_next ? ids_nxt[b] : ids_cur[b], issue_j);
+      const int g = issue_in_next ? nxt.g : cur.g;
       if (lane == 0) {
-        const uint32_t stage = (used + k) % STAGES;
-        const uint32_t bar = warp_bar + 8 * stage;
-        const uint32_t kdst = warp_pipe + stage * C::STAGE;
-        const uint32_t vdst = kdst + KH * C::TILE;
+        const uint32_t st = issued % STAGES;
+        const uint32_t fb = my_bar + 8 * st;
         int nload = 0;
 #pragma unroll
-        for (int b = 0; b < BPU; ++b) nload += bid[b] >= 0;
+        for (int b = 0; b < BOXES; ++b) nload += bid[b] >= 0;
         if (nload == 0) {
-          mbar_arrive(bar);
+          mbar_arrive(fb);
         } else {
-          mbar_arrive_expect_tx(bar, (uint32_t)nload * 2 * KH * BS * 128);
+          mbar_arrive_expect_tx(fb, (uint32_t)nload * 2 * C::BOX_BYTES);
+          const uint32_t kdst = my_pipe + st * C::STAGE;
+          const uint32_t vdst = kdst + C::KV_BYTES;
 #pragma unroll
-          for (int b = 0; b < BPU; ++b) {
+          for (int b = 0; b < BOXES; ++b) {
             if (bid[b] < 0) continue;
-            const int32_t y = (bid[b] * a.n_kv + g) * BS;
+            // first row of this box: block row base plus the 16-token
+            // window's offset inside a 32-token block
+            const int tok_in_block = ((issue_in_next ? nxt.u_begin : cur.u_begin) +
+                                      warp + issue_j * kWarps) * kUnit % BS + b * ROWS;
+            const int32_t y = (bid[b] * a.n_kv + g) * BS + (BS > kUnit ? tok_in_block : 0);
+            if (KH == 2 && a.map3d) {
+              tma_load_3d(kdst + b * C::BOX_BYTES, &tmk, 0, y, 0, fb);
+              tma_load_3d(vdst + b * C::BOX_BYTES, &tmv, 0, y, 0, fb);
+            } else {
 #pragma unroll
-            for (int h = 0; h < KH; ++h) {
-              tma_load_2d(kdst + h * C::TILE + b * BS * 128, &tmk, h * 64, y, bar);
-              tma_load_2d(vdst + h * C::TILE + b * BS * 128, &tmv, h * 64, y, bar);
+              for (int h = 0; h < KH; ++h) {
+                tma_load_2d(kdst + b * C::BOX_BYTES + h * ROWS * 128, &tmk, h * 64, y, fb);
+                tma_load_2d(vdst + b * C::BOX_BYTES + h * ROWS * 128, &tmv, h * 64, y, fb);
+              }
             }
           }
         }
       }
-    };
+      ++issued;
+      ++issue_j;
+    }
+  };
 
 #pragma unroll 1
-    for (int k = 0; k < STAGES; ++k)
-      if (k < n_w) issue(k);
+  for (int k = 0; have_cur; ++k) {
+    PA_EVENT(2);
+    // ---- fetch item k + 2 of this CTA; the value is only needed after the
+    // merge, so it is published then and its latency hides behind the units
+    int fetched = INT_MAX;
+    if (tid == 0 && have_nxt) fetched = 2 * (int)gridDim.x + atomicAdd(&a.work[0], 1);
 
-    // ---- query fragments (B operand: head_dim x heads, column-major = q rows)
-    uint32_t qf[NT][KS][2];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int n = t * 8 + (lane >> 2);
-      const bool real = n < a.group;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          a.q + ((int64_t)s * a.n_q + g * a.group + (real ? n : 0)) * D);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qf[t][ks][0] = real ? __ldg(&qrow[ks * 8 + (lane & 3)]) : 0u;
-        qf[t][ks][1] = real ? __ldg(&qrow[ks * 8 + 4 + (lane & 3)]) : 0u;
-      }
-    }
-
+    // ---- stream this warp's units of the current item
     float acc[NT][KS][4];
     float mrun[NT][2], lrun[NT][2];
 #pragma unroll
@@ -276,117 +399,112 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       mrun[t][0] = mrun[t][1] = -INFINITY;
       lrun[t][0] = lrun[t][1] = 0.f;
     }
-
+    const int n_mine = units_of_warp(cur, warp);
 #pragma unroll 1
-    for (int k = 0; k < n_w; ++k) {
-      const uint32_t idx = used + k;
-      const uint32_t stage = idx % STAGES;
-      if (!mbar_wait_bounded(warp_bar + 8 * stage, (idx / STAGES) & 1u, kWaitLimitNs)) {
-        if (lane == 0) {
-          report(a.err, PA_DEV_ERR_TIMEOUT);
-          misc[2] = 1;
-        }
-        drain_from = used + k;
-        drain_to = used + min(n_w, k + STAGES);
-        break;
-      }
-      const int u = u_begin + warp + k * kWarps;
-      const int nv = min(ST, tok_end - u * ST);  // valid tokens in this unit
-      int bid[BPU];
-      bool all_ok = nv == ST;
+    for (int j = 0; j < n_mine; ++j) {
+      fill();
+      const uint32_t st = consumed % STAGES;
+      wait_or_flag(my_bar + 8 * st, (consumed / STAGES) & 1u, a, fault);
+      int mask = 0;
 #pragma unroll
-      for (int b = 0; b < BPU; ++b) {
-        bid[b] = __shfl_sync(0xffffffffu, ids[b], k);
-        if (b * BS < nv && bid[b] < 0) all_ok = false;
-      }
-      const uint32_t kb = warp_pipe + stage * C::STAGE;
-      const uint32_t vb = kb + KH * C::TILE;
+      for (int b = 0; b < BOXES; ++b)
+        mask |= (__shfl_sync(0xffffffffu, ids_cur[b], j) >= 0 ? 1 : 0) << b;
+      const int nv = min(kUnit, cur.tok_end - (cur.u_begin + warp + j * kWarps) * kUnit);
+      const uint32_t kb = my_pipe + st * C::STAGE;
+      const uint32_t vb = kb + C::KV_BYTES;
+      bool all_ok = nv == kUnit;
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b)
+        if (b * ROWS < nv && !(mask >> b & 1)) all_ok = false;
       if (!all_ok) {
-        // Rows of absent tokens may hold anything (even NaN): zero their V so
-        // that a zero weight times the row stays zero.
-        uint8_t* vgen = smem + (vb - smem_base);
-        for (int i = lane; i < ST * KH * 8; i += 32) {
+        // Rows of absent tokens may hold anything (even NaN): zero their V
+        // so that a zero weight times the row stays zero.
+        uint8_t* vgen = smem + (vb - sbase);
+        for (int i = lane; i < kUnit * KH * 8; i += 32) {
           const int r = i / (KH * 8), rest = i % (KH * 8);
           const int h = rest / 8, c = rest % 8;
-          if (r >= nv || bid[r / BS] < 0)
-            *reinterpret_cast<uint4*>(vgen + h * C::TILE + r * 128 + c * 16) =
-                make_uint4(0, 0, 0, 0);
+          if (r >= nv || !(mask >> (r / ROWS) & 1))
+            *reinterpret_cast<uint4*>(vgen + (r / ROWS) * C::BOX_BYTES + h * ROWS * 128 +
+                                      (r % ROWS) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();
         __syncwarp();
       }
 
+      // ---- S^T = K Q^T for 16 tokens x 8 heads (per n-tile)
+      float sc[NT][4];
 #pragma unroll
-      for (int mt = 0; mt < ST / 16; ++mt) {
-        if (mt * 16 >= nv) break;
-        // ---- S^T = K Q^T for 16 tokens x 8 heads (per n-tile)
-        float sc[NT][4];
+      for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+      {
+        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t row = kb + (r / ROWS) * C::BOX_BYTES + (r % ROWS) * 128;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-        {
-          const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        for (int ks = 0; ks < KS; ++ks) {
+          const int h = ks >> 2;
+          const int c = ((ks & 3) << 1) + (lane >> 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const int h = ks >> 2;
-            const int c = ((ks & 3) << 1) + (lane >> 4);
-            const uint32_t addr = kb + h * C::TILE + r * 128 + ((c ^ (r & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-              mma_bf16_16816(sc[t], a0, a1, a2, a3, qf[t][ks][0], qf[t][ks][1]);
-          }
-        }
-        // ---- mask, online softmax (base 2), P^T fragments
-        const int tA = mt * 16 + (lane >> 2), tB = tA + 8;
-        const bool okA = tA < nv && bid[tA / BS] >= 0;
-        const bool okB = tB < nv && bid[tB / BS] >= 0;
-        uint32_t pb[NT][2];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          float pv[4];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float xa = okA ? sc[t][j] * a.scale_log2 : -INFINITY;
-            const float xb = okB ? sc[t][j + 2] * a.scale_log2 : -INFINITY;
-            const float mx = warp_max_xor4(fmaxf(xa, xb));
-            const float m_new = fmaxf(mrun[t][j], mx);
-            const float base = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(mrun[t][j] - base);
-            pv[j] = fast_exp2(xa - base);
-            pv[j + 2] = fast_exp2(xb - base);
-            lrun[t][j] = lrun[t][j] * alpha + pv[j] + pv[j + 2];
-            mrun[t][j] = m_new;
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-              acc[t][dt][j] *= alpha;
-              acc[t][dt][j + 2] *= alpha;
-            }
-          }
-          pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
-          pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
-        }
-        // ---- O^T += V^T P^T
-        {
-          const int mi = lane >> 3;
-          const int r = mt * 16 + (lane & 7) + (mi >> 1) * 8;
-#pragma unroll
-          for (int dt = 0; dt < KS; ++dt) {
-            const int h = dt >> 2;
-            const int c = ((dt & 3) << 1) + (mi & 1);
-            const uint32_t addr = vb + h * C::TILE + r * 128 + ((c ^ (r & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(addr, a0, a1, a2, a3);
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-              mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
-          }
+          for (int t = 0; t < NT; ++t)
+            mma_bf16_16816(sc[t], a0, a1, a2, a3, qf_cur[t][ks][0], qf_cur[t][ks][1]);
         }
       }
+      // ---- mask, online softmax (base 2), P^T fragments
+      const int tA = lane >> 2, tB = tA + 8;
+      const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
+      const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float pv[4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const float xa = okA ? sc[t][jj] * a.scale_log2 : -INFINITY;
+          const float xb = okB ? sc[t][jj + 2] * a.scale_log2 : -INFINITY;
+          const float mx = warp_max_xor4(fmaxf(xa, xb));
+          const float m_new = fmaxf(mrun[t][jj], mx);
+          const float base = m_new == -INFINITY ? 0.f : m_new;
+          const float alpha = fast_exp2(mrun[t][jj] - base);
+          pv[jj] = fast_exp2(xa - base);
+          pv[jj + 2] = fast_exp2(xb - base);
+          lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
+          mrun[t][jj] = m_new;
+#pragma unroll
+          for (int dt = 0; dt < KS; ++dt) {
+            acc[t][dt][jj] *= alpha;
+            acc[t][dt][jj + 2] *= alpha;
+          }
+        }
+        pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
+        pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
+      }
+      // ---- O^T += V^T P^T
+      {
+        const int mi = lane >> 3;
+        const int r = (lane & 7) + (mi >> 1) * 8;
+        const uint32_t row = vb + (r / ROWS) * C::BOX_BYTES + (r % ROWS) * 128;
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+          const int h = dt >> 2;
+          const int c = ((dt & 3) << 1) + (mi & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+        }
+      }
+      // The stage is refilled by this warp's next fill(); generic writes to
+      // it (the zeroed rows) must be ordered before that TMA.
+      if (!all_ok) fence_proxy_async_smem();
       __syncwarp();
-      if (k + STAGES < n_w) issue(k + STAGES);
+      ++consumed;
     }
-    used += n_w;
+    fill();  // the next item's first units fly while the CTA merges
+    PA_EVENT(3);
+    if (tid == 0) {
+      mail[k & 3] = fetched;
+      mbar_arrive(mail_bar + 8 * (k & 3));
+    }
 
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -394,124 +512,207 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       lrun[t][1] = warp_sum_xor4(lrun[t][1]);
     }
 
-    __syncthreads();  // every warp is done with its stages; the buffers are free
-    if (misc[2]) break;
-
-    // ---- cross-warp merge through shared memory
-    float* macc = reinterpret_cast<float*>(smem);
-    float* mm = macc + kWarps * C::HEADS * C::MSTRIDE;
-    float* ml = mm + kWarps * C::HEADS;
+    // ---- merge: warps 1-3 hand their state to warp 0 through shared memory
+    if (warp > 0) {
+      float* buf = macc + (warp - 1) * G * C::MSTRIDE;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
+      for (int t = 0; t < NT; ++t) {
 #pragma unroll
-      for (int dt = 0; dt < KS; ++dt)
+        for (int dt = 0; dt < KS; ++dt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int n = t * 8 + 2 * (lane & 3) + (i & 1);
-          const int d = dt * 16 + (lane >> 2) + 8 * (i >> 1);
-          macc[(warp * C::HEADS + n) * C::MSTRIDE + d] = acc[t][dt][i];
+          for (int i = 0; i < 4; ++i) {
+            const int n = t * 8 + 2 * (lane & 3) + (i & 1);
+            const int d = dt * 16 + (lane >> 2) + 8 * (i >> 1);
+            if (n < G) buf[n * C::MSTRIDE + d] = acc[t][dt][i];
+          }
+        if (lane < 4) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int n = t * 8 + 2 * lane + jj;
+            mlb[((warp - 1) * C::HEADS + n) * 2] = mrun[t][jj];
+            mlb[((warp - 1) * C::HEADS + n) * 2 + 1] = lrun[t][jj];
+          }
         }
-      if (lane < 4) {
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll 1
+      for (int w = 0; w < kWarps - 1; ++w) {
+        const float* buf = macc + w * G * C::MSTRIDE;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          mm[warp * C::HEADS + t * 8 + 2 * lane + j] = mrun[t][j];
-          ml[warp * C::HEADS + t * 8 + 2 * lane + j] = lrun[t][j];
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int n = t * 8 + 2 * (lane & 3) + jj;
+            if (n >= G) continue;
+            const float mo = mlb[(w * C::HEADS + n) * 2];
+            const float lo = mlb[(w * C::HEADS + n) * 2 + 1];
+            const float M = fmaxf(mrun[t][jj], mo);
+            const float es = mrun[t][jj] == -INFINITY ? 0.f : fast_exp2(mrun[t][jj] - M);
+            const float eo = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+            lrun[t][jj] = es * lrun[t][jj] + eo * lo;
+            mrun[t][jj] = M;
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+              const int d = dt * 16 + (lane >> 2);
+              acc[t][dt][jj] = es * acc[t][dt][jj] + eo * buf[n * C::MSTRIDE + d];
+              acc[t][dt][jj + 2] = es * acc[t][dt][jj + 2] + eo * buf[n * C::MSTRIDE + d + 8];
+            }
+          }
+        }
+      }
+      // the CTA's result for the item, back into buffer 0 for coalesced writes
+      float* buf = macc;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = t * 8 + 2 * (lane & 3) + (i & 1);
+            const int d = dt * 16 + (lane >> 2) + 8 * (i >> 1);
+            if (n < G) buf[n * C::MSTRIDE + d] = acc[t][dt][i];
+          }
+        if (lane < 4) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            fin[t * 8 + 2 * lane + jj] = mrun[t][jj];
+            fin[16 + t * 8 + 2 * lane + jj] = lrun[t][jj];
+          }
         }
       }
     }
     __syncthreads();
 
-    const int G = a.group;
-    const int64_t row0 = (int64_t)s * a.n_q + (int64_t)g * G;
+    PA_EVENT(4);
+    const int64_t row0 = (int64_t)cur.s * a.n_q + (int64_t)cur.g * G;
     for (int i = tid; i < G * D; i += kThreads) {
       const int n = i / D, d = i - n * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * C::HEADS + n]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = mm[w * C::HEADS + n];
-        const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-        L += e * ml[w * C::HEADS + n];
-        O += e * macc[(w * C::HEADS + n) * C::MSTRIDE + d];
-      }
-      if (nparts == 1) {
+      const float O = macc[n * C::MSTRIDE + d];
+      const float M = fin[n], L = fin[16 + n];
+      if (cur.nparts == 1) {
         a.out[(row0 + n) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
       } else {
-        const int64_t wr = (row0 + n) * a.max_parts + p;
+        const int64_t wr = (row0 + n) * a.max_parts + cur.p;
         a.ws_o[wr * D + d] = O;
         if (d == 0) a.ws_ml[wr] = make_float2(M, L);
       }
     }
 
-    if (nparts > 1) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        int32_t* tk = &a.tickets[(int64_t)s * a.n_kv + g];
-        const int done = atomicAdd(tk, 1);
-        const int last = done == nparts - 1;
-        if (last) atomicExch(tk, 0);  // every partition has checked in: reset
-        misc[1] = last;
+    __syncthreads();  // merge buffer, fin and misc are free again
+    PA_EVENT(6);
+
+    // ---- advance: the next item becomes current; learn the one after it
+    have_cur = have_nxt;
+    if (!have_cur) break;
+    cur = nxt;
+#pragma unroll
+    for (int b = 0; b < BOXES; ++b) ids_cur[b] = ids_nxt[b];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf_cur[t][ks][0] = qf_nxt[t][ks][0];
+        qf_cur[t][ks][1] = qf_nxt[t][ks][1];
       }
-      __syncthreads();
-      if (misc[1]) {
-        __threadfence();
-        // log-sum-exp weights per head and partition: w_p = 2^(m_p - M) / L
-        float* wts = reinterpret_cast<float*>(smem);
-        for (int n = warp; n < G; n += kWarps) {
-          const float2* mlp = a.ws_ml + (row0 + n) * a.max_parts;
-          float M = -INFINITY;
-          for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&mlp[q]).x);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          float L = 0.f;
-          for (int q = lane; q < nparts; q += 32) {
-            const float2 v = __ldcg(&mlp[q]);
-            L += v.x == -INFINITY ? 0.f : fast_exp2(v.x - M) * v.y;
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          for (int q = lane; q < nparts; q += 32) {
-            const float mq = __ldcg(&mlp[q]).x;
-            wts[n * a.max_parts + q] = mq == -INFINITY ? 0.f : fast_exp2(mq - M) * inv;
-          }
-        }
-        __syncthreads();
-        for (int i = tid; i < G * D; i += kThreads) {
-          const int n = i / D, d = i - n * D;
-          const float* op = a.ws_o + (row0 + n) * a.max_parts * D + d;
-          const float* wn = wts + n * a.max_parts;
-          float O0 = 0.f, O1 = 0.f;
-          int q = 0;
-          for (; q + 1 < nparts; q += 2) {
-            O0 += wn[q] * __ldcg(op + (int64_t)q * D);
-            O1 += wn[q + 1] * __ldcg(op + (int64_t)(q + 1) * D);
-          }
-          if (q < nparts) O0 += wn[q] * __ldcg(op + (int64_t)q * D);
-          a.out[(row0 + n) * D + d] = __float2bfloat16_rn(O0 + O1);
-        }
+    if (issue_in_next) {
+      issue_in_next = 0;  // the issue cursor already runs inside the new current item
+    } else {
+      issue_j = 0;
+    }
+    {
+      // the new next item is this CTA's item k + 2, fetched at the top of
+      // this iteration into mailbox slot k mod 4
+      const int slot = k & 3;
+      wait_or_flag(mail_bar + 8 * slot, (k >> 2) & 1u, a, fault);
+      const int item_n = mail[slot];
+      have_nxt = item_n < total;
+      if (have_nxt) {
+        nxt = decode_item(item_n, prefix, a);
+        load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
+        load_q<D, NT>(qf_nxt, nxt, lane, a);
       }
     }
-
-    fence_proxy_async_smem();  // generic writes above precede the next TMA loads
-    if (tid == 0) misc[0] = next;
-    __syncthreads();
-    item = misc[0];
   }
 
-  // After a timeout, let this warp's copies still in flight land (bounded)
-  // before the CTA exits.
-  for (uint32_t i = drain_from; i < drain_to; ++i)
-    mbar_wait_bounded(warp_bar + 8 * (i % STAGES), (i / STAGES) & 1u, 100000000ull);
+  __syncthreads();
+  PA_EVENT(7);
+  griddep_launch_dependents();  // the partition merge may start launching
   if (tid == 0) {
-    const int fin = atomicAdd(&a.work[1], 1);
-    if (fin == (int)gridDim.x - 1) {  // the last CTA resets the shared counters
+    const int fin_ctas = atomicAdd(&a.work[1], 1);
+    if (fin_ctas == (int)gridDim.x - 1) {  // the last CTA resets the shared counters
       atomicExch(&a.work[0], 0);
       atomicExch(&a.work[1], 0);
     }
+  }
+}
+
+// Merge of split-KV partitions: one warp per (sequence, query head) row with
+// more than one partition; lanes own head_dim columns. With m_p, l_p the
+// running max (log2 units) and sum of partition p and O_p its unnormalised
+// output: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
+struct MergeArgs {
+  __nv_bfloat16* out;
+  const float* ws_o;
+  const float2* ws_ml;
+  const int32_t* seq_lens;
+  int num_seqs, n_q, part_tokens, max_parts, len_cap;
+};
+
+constexpr int kMergeWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs m) {
+  griddep_wait();  // the partitions come from the decode grid
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int rows = m.num_seqs * m.n_q;
+  for (int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5); row < rows;
+       row += gridDim.x * kMergeWarps) {
+    const int s = row / m.n_q;
+    const int nparts = parts_of(clamp_len(__ldg(&m.seq_lens[s]), m.len_cap), m.part_tokens);
+    if (nparts <= 1) continue;  // written directly by the decode kernel
+    const float2* ml = m.ws_ml + (int64_t)row * m.max_parts;
+    float M = -INFINITY;
+    for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&ml[q]).x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int q = lane; q < nparts; q += 32) {
+      const float2 v = __ldcg(&ml[q]);
+      L += v.x == -INFINITY ? 0.f : fast_exp2(v.x - M) * v.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float* op = m.ws_o + (int64_t)row * m.max_parts * D + lane;
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    int q = 0;
+    for (; q + 1 < nparts; q += 2) {
+      const float m0 = __ldcg(&ml[q]).x, m1 = __ldcg(&ml[q + 1]).x;
+      float o0[PER], o1[PER];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        o0[i] = __ldcg(op + (int64_t)q * D + 32 * i);
+        o1[i] = __ldcg(op + (int64_t)(q + 1) * D + 32 * i);
+      }
+      const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += w0 * o0[i] + w1 * o1[i];
+    }
+    if (q < nparts) {
+      const float mq = __ldcg(&ml[q]).x;
+      const float w = mq == -INFINITY ? 0.f : fast_exp2(mq - M);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += w * __ldcg(op + (int64_t)q * D + 32 * i);
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      m.out[(int64_t)row * D + lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
   }
 }
 
@@ -531,35 +732,59 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool as a 2-D bf16 tensor [num_blocks * n_kv * bs rows][D columns];
-// one box is 64 columns (128 bytes, the swizzle span) by block_size rows.
-static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows, int bs) {
+// The pool as bf16 rows of D columns (num_blocks * n_kv * bs rows); a box
+// is `box_rows` rows of 64 columns (128 bytes, the swizzle span). For
+// D = 128 a 3-D view (64 columns, rows, 2 halves 128 bytes apart) lets one
+// copy fetch both halves of the rows; *map3d says which view was built.
+static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
+                               int box_rows, bool try3d, int* map3d) {
   auto fn = encode_fn();
   if (!fn) return cuda_fail_msg("pa_decode", "cuTensorMapEncodeTiled unavailable");
+  if (try3d && D == 128) {
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+      *map3d = 1;
+      return PA_OK;
+    }
+  }
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)bs};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail_msg("pa_decode", "cuTensorMapEncodeTiled failed");
+  *map3d = 0;
   return PA_OK;
 }
 
 template <int D, int BS, int NT>
-static pa_status launch(const DecodeArgs& a, const void* k_pool, const void* v_pool,
+static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
                         int64_t items_upper, cudaStream_t stream) {
   using C = Cfg<D, BS, NT>;
   auto kern = decode_kernel<D, BS, NT>;
   const int64_t rows = (int64_t)a.num_blocks * a.n_kv * BS;
   CUtensorMap tmk, tmv;
-  pa_status st = make_pool_map(&tmk, k_pool, D, rows, BS);
+  int k3 = 0, v3 = 0;
+  pa_status st = make_pool_map(&tmk, k_pool, D, rows, C::ROWS, true, &k3);
   if (st != PA_OK) return st;
-  st = make_pool_map(&tmv, v_pool, D, rows, BS);
+  st = make_pool_map(&tmv, v_pool, D, rows, C::ROWS, k3 == 1, &v3);
   if (st != PA_OK) return st;
+  if (k3 != v3) {  // both views must agree
+    st = make_pool_map(&tmk, k_pool, D, rows, C::ROWS, false, &k3);
+    if (st != PA_OK) return st;
+  }
+  a.map3d = k3 && v3;
 
-  const size_t smem = C::smem_bytes(a.num_seqs);
+  const size_t smem = C::smem_bytes(a.num_seqs, a.group);
   static int configured = 0;  // largest dynamic smem size already allowed
   static int occ_for_smem[2] = {-1, 0};
   if ((int)smem > configured) {
@@ -581,9 +806,44 @@ static pa_status launch(const DecodeArgs& a, const void* k_pool, const void* v_p
   int64_t grid = (int64_t)num_sms() * occ;
   if (grid > items_upper) grid = items_upper;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, smem, stream>>>(tmk, tmv, a);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? PA_OK : cuda_fail("pa_decode launch", e);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
+  if (e != cudaSuccess) return cuda_fail("pa_decode launch", e);
+  if (a.max_parts > 1) {
+    MergeArgs m;
+    m.out = a.out;
+    m.ws_o = a.ws_o;
+    m.ws_ml = a.ws_ml;
+    m.seq_lens = a.seq_lens;
+    m.num_seqs = a.num_seqs;
+    m.n_q = a.n_q;
+    m.part_tokens = a.part_tokens;
+    m.max_parts = a.max_parts;
+    m.len_cap = a.len_cap;
+    const int64_t rows = (int64_t)a.num_seqs * a.n_q;
+    int64_t mgrid = (rows + kMergeWarps - 1) / kMergeWarps;
+    const int64_t mcap = (int64_t)num_sms() * 8;
+    if (mgrid > mcap) mgrid = mcap;
+    cudaLaunchConfig_t mc = {};
+    mc.gridDim = dim3((unsigned)mgrid);
+    mc.blockDim = dim3(kMergeWarps * 32);
+    mc.dynamicSmemBytes = 0;
+    mc.stream = stream;
+    mc.attrs = attr;
+    mc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&mc, merge_kernel<D>, m);
+    if (e != cudaSuccess) return cuda_fail("pa_decode merge launch", e);
+  }
+  return PA_OK;
 }
 
 template <int D, int BS>
@@ -603,16 +863,17 @@ static pa_status dispatch_bs(int bs, const DecodeArgs& a, const void* kp, const 
   }
 }
 
-static int stage_tokens(int block_size) { return block_size < 16 ? 16 : block_size; }
-
-// Partition size: explicit, or the largest of 512/256/128/64 tokens that
-// still gives the persistent grid (about 2 CTAs on each of ~150 SMs) several
-// items each, estimating the mean length as half the maximum.
+// Partition size: explicit (a multiple of the 16-token unit, at most 2048),
+// or the largest of 512/256/128/64 tokens that still gives the persistent
+// grid (about 2 CTAs on each of ~150 SMs) several items each, estimating the
+// mean length as half the maximum.
 static int resolve_partition(int num_seqs, int n_kv, int block_size, int max_seq_len,
                              int partition_tokens) {
-  const int st = stage_tokens(block_size);
+  (void)block_size;
+  const int st = kUnit;
   if (partition_tokens != 0) {
-    if (partition_tokens < st || partition_tokens % st != 0 || partition_tokens > 128 * st)
+    if (partition_tokens < st || partition_tokens % st != 0 ||
+        partition_tokens > kMaxUnitsPerPart * st)
       return -1;
     return partition_tokens;
   }
@@ -629,7 +890,7 @@ static int resolve_partition(int num_seqs, int n_kv, int block_size, int max_seq
 }
 
 struct WsLayout {
-  size_t o_off, ml_off, tick_off, work_off, total;
+  size_t o_off, ml_off, work_off, total;
   int max_parts;
 };
 
@@ -641,9 +902,9 @@ static bool layout(int num_seqs, int n_q, int n_kv, int D, int P, int max_seq_le
   w->max_parts = (int)mp;
   const size_t rows = (size_t)num_seqs * n_q * mp;
   w->o_off = 0;
+  (void)n_kv;
   w->ml_off = align256(rows * D * sizeof(float));
-  w->tick_off = w->ml_off + align256(rows * sizeof(float2));
-  w->work_off = w->tick_off + align256((size_t)num_seqs * n_kv * sizeof(int32_t));
+  w->work_off = w->ml_off + align256(rows * sizeof(float2));
   w->total = w->work_off + 256;
   return true;
 }
@@ -714,7 +975,6 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   a.seq_lens = seq_lens;
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
   a.ws_ml = reinterpret_cast<float2*>(ws + w.ml_off);
-  a.tickets = reinterpret_cast<int32_t*>(ws + w.tick_off);
   a.work = reinterpret_cast<int32_t*>(ws + w.work_off);
   a.err = err_word;
   a.num_seqs = num_seqs;
@@ -727,6 +987,7 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   a.max_parts = w.max_parts;
   a.len_cap = max_seq_len;
   a.scale_log2 = scale * kLog2e;
+  a.map3d = 0;
   const int64_t items_upper = (int64_t)num_seqs * n_kv_heads * w.max_parts;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 64) return dispatch_bs<64>(block_size, a, k_pool, v_pool, items_upper, st);
@@ -773,6 +1034,17 @@ static void* noalloc_scratch(pa_status* st) {
 
 }  // namespace pa
 
+#ifdef PA_TRACE
+extern "C" int pa_trace_read(uint64_t* host, int* counts) {
+  if (cudaMemcpyFromSymbol(host, pa::g_trace, sizeof(pa::g_trace)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(counts, pa::g_trace_n, sizeof(pa::g_trace_n)) != cudaSuccess)
+    return -1;
+  static int zeros[1024] = {0};
+  if (cudaMemcpyToSymbol(pa::g_trace_n, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  return pa::kTraceSlots;
+}
+#endif
+
 extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool,
                                        const void* v_pool, const int32_t* block_tables,
                                        const int32_t* seq_lens, int num_seqs,
@@ -794,16 +1066,16 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_p
   pa_status st = PA_OK;
   void* scratch = noalloc_scratch(&st);
   if (scratch == nullptr) return st;
-  // The tickets and work counters must start at zero. A completed call
-  // leaves them zeroed, but the array is shared by every call in the
-  // process, so clear them here rather than trust the previous caller.
+  // The work counters must start at zero. A completed call leaves them
+  // zeroed, but the array is shared by every call in the process, so clear
+  // them here rather than trust the previous caller.
   const int P = resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len,
                                   partition_tokens);
   WsLayout w;
   if (P <= 0 || !layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
     return PA_ERR_UNSUPPORTED;
-  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.tick_off, 0,
-                                  w.total - w.tick_off, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.work_off, 0,
+                                  w.total - w.work_off, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("pa_decode_noalloc memset", e);
   return pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
                    max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim, block_size,

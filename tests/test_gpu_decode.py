@@ -92,6 +92,13 @@ def test_partition_sizes_agree(P):
     full_parity(wl, partition_tokens=P)
 
 
+@pytest.mark.parametrize("P", [16, 48, 80, 1008])
+def test_partitions_splitting_32_token_blocks(P):
+    wl = W.custom([1, 17, 47, 100, 333, 1500], block_size=32, n_q_heads=8, n_kv_heads=2,
+                  head_dim=128, seed=P)
+    full_parity(wl, partition_tokens=P)
+
+
 def test_empty_sequences_give_zeros():
     wl = W.custom([0, 5, 0, 300, 0], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=64,
                   seed=9)
