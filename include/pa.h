@@ -137,7 +137,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  *   block_tables       int32 [num_seqs][max_blocks_per_seq]; only the first
  *                      ceil(len_s / block_size) entries of row s are read
  *   seq_lens           int32 [num_seqs]
- *   num_seqs           >= 0 (0: nothing is launched), <= 16384
+ *   num_seqs           >= 0 (0: nothing is launched), <= 8192
  *   max_blocks_per_seq >= 1 (row stride of block_tables)
  *   num_blocks         >= 1, num_blocks*n_kv_heads*block_size < 2^31
  *   n_q_heads, n_kv_heads  >= 1, n_q_heads % n_kv_heads == 0, G <= 16

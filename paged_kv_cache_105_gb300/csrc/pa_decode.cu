@@ -47,6 +47,9 @@
 
 namespace pa {
 
+#ifndef PA_WARP_BUDGET
+#define PA_WARP_BUDGET 16384
+#endif
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnit = 16;                           // tokens per pipeline stage
@@ -54,7 +57,7 @@ constexpr int kMaxUnitsPerPart = 128;               // lane-held table entries: 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s: a wait that long is a fault
 constexpr uint64_t kWaitAfterFaultNs = 1000000ull;  // 1 ms once something has timed out
 constexpr int kMaxParts = 1024;
-constexpr int kMaxSeqs = 16384;
+constexpr int kMaxSeqs = 8192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -80,7 +83,7 @@ struct Cfg {
   static constexpr int BOX_BYTES = KH * ROWS * 128;     // one box of K (or V), all halves
   static constexpr int KV_BYTES = BOXES * BOX_BYTES;    // K (or V) of a unit = 16 * D * 2
   static constexpr int STAGE = 2 * KV_BYTES;
-  static constexpr int BUDGET = NT == 1 ? 24576 : 16384;  // pipeline bytes per warp
+  static constexpr int BUDGET = NT == 1 ? PA_WARP_BUDGET : 16384;  // pipeline bytes per warp
   static constexpr int STAGES_RAW = BUDGET / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr int HEADS = NT * 8;
@@ -98,9 +101,10 @@ struct Cfg {
   __host__ __device__ static int prefix_off(int group) {
     return MERGE_OFF + 3 * group * MSTRIDE * 4;
   }
+  // prefix[num_seqs + 1] then the clamped lengths lens[num_seqs]
   static size_t smem_bytes(int num_seqs, int group) {
     return 1024 /* alignment slack */ + prefix_off(group) +
-           sizeof(int) * (size_t)(num_seqs + 1);
+           sizeof(int) * (size_t)(2 * num_seqs + 1);
   }
 };
 
@@ -126,8 +130,9 @@ __device__ __forceinline__ float warp_sum_xor4(float v) {
   return v;
 }
 
-// Exclusive prefix over sequences of the item count n_kv * parts(len).
-__device__ void build_prefix(int* prefix, const DecodeArgs& a, int* warp_tot) {
+// Exclusive prefix over sequences of the item count n_kv * parts(len), and
+// the clamped lengths, both kept in shared memory for item lookups.
+__device__ void build_prefix(int* prefix, int* lens, const DecodeArgs& a, int* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (a.num_seqs + kThreads - 1) / kThreads;
   const int b = min(a.num_seqs, tid * per), e = min(a.num_seqs, b + per);
@@ -136,6 +141,7 @@ __device__ void build_prefix(int* prefix, const DecodeArgs& a, int* warp_tot) {
     const int raw = __ldg(&a.seq_lens[s]);
     const int len = clamp_len(raw, a.len_cap);
     if (raw != len && blockIdx.x == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
+    lens[s] = len;
     sum += a.n_kv * parts_of(len, a.part_tokens);
   }
   int incl = sum;
@@ -151,7 +157,7 @@ __device__ void build_prefix(int* prefix, const DecodeArgs& a, int* warp_tot) {
   int run = base + incl - sum;
   for (int s = b; s < e; ++s) {
     prefix[s] = run;
-    run += a.n_kv * parts_of(clamp_len(__ldg(&a.seq_lens[s]), a.len_cap), a.part_tokens);
+    run += a.n_kv * parts_of(lens[s], a.part_tokens);
   }
   if (tid == kThreads - 1) prefix[a.num_seqs] = base + incl;
 }
@@ -172,7 +178,8 @@ struct Item {
   int s, g, p, nparts, tok_end, u_begin, n_units;
 };
 
-__device__ __forceinline__ Item decode_item(int item, const int* prefix, const DecodeArgs& a) {
+__device__ __forceinline__ Item decode_item(int item, const int* prefix, const int* lens,
+                                            const DecodeArgs& a) {
   int lo = 0, hi = a.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -184,7 +191,7 @@ __device__ __forceinline__ Item decode_item(int item, const int* prefix, const D
   const int local = item - prefix[lo];
   it.g = local / it.nparts;
   it.p = local - it.g * it.nparts;
-  const int len = clamp_len(__ldg(&a.seq_lens[lo]), a.len_cap);
+  const int len = lens[lo];
   const int tok_begin = it.p * a.part_tokens;
   it.tok_end = min(len, tok_begin + a.part_tokens);
   it.u_begin = tok_begin / kUnit;
@@ -276,6 +283,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   float* mlb = reinterpret_cast<float*>(smem + C::ML_OFF);
   float* macc = reinterpret_cast<float*>(smem + C::MERGE_OFF);
   int* prefix = reinterpret_cast<int*>(smem + C::prefix_off(a.group));
+  int* lens = prefix + a.num_seqs + 1;
   volatile int* fault = misc + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -292,7 +300,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     prefetch_tensormap(&tmv);
   }
   griddep_wait();  // inputs may come from the previous kernel on the stream
-  build_prefix(prefix, a, reinterpret_cast<int*>(smem + C::ML_OFF));
+  build_prefix(prefix, lens, a, reinterpret_cast<int*>(smem + C::ML_OFF));
   __syncthreads();
   const int total = prefix[a.num_seqs];
   const int G = a.group;
@@ -307,13 +315,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   bool have_cur = item < total;
   bool have_nxt = false;
   if (have_cur) {
-    cur = decode_item(item, prefix, a);
+    cur = decode_item(item, prefix, lens, a);
     load_ids<BS, BOXES, ROWS>(ids_cur, cur, warp, lane, a);
     load_q<D, NT>(qf_cur, cur, lane, a);
     const int item1 = item + (int)gridDim.x;
     have_nxt = item1 < total;
     if (have_nxt) {
-      nxt = decode_item(item1, prefix, a);
+      nxt = decode_item(item1, prefix, lens, a);
       load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
       load_q<D, NT>(qf_nxt, nxt, lane, a);
     }
@@ -629,7 +637,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       const int item_n = mail[slot];
       have_nxt = item_n < total;
       if (have_nxt) {
-        nxt = decode_item(item_n, prefix, a);
+        nxt = decode_item(item_n, prefix, lens, a);
         load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
         load_q<D, NT>(qf_nxt, nxt, lane, a);
       }

@@ -99,6 +99,14 @@ def test_partitions_splitting_32_token_blocks(P):
     full_parity(wl, partition_tokens=P)
 
 
+def test_many_short_sequences():
+    # thousands of sequences: the per-sequence prefix table is large
+    rng = np.random.default_rng(77)
+    lens = rng.integers(0, 40, size=3000).tolist()
+    wl = W.custom(lens, block_size=8, n_q_heads=4, n_kv_heads=1, head_dim=64, seed=77)
+    full_parity(wl)
+
+
 def test_empty_sequences_give_zeros():
     wl = W.custom([0, 5, 0, 300, 0], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=64,
                   seed=9)
