@@ -87,9 +87,9 @@ const char* pa_last_cuda_error(void);
 /*
  * Partition size pa_decode uses, in tokens: `partition_tokens` itself when
  * non-zero (checked: a multiple of 16, at most 2048; a partition may start
- * inside a 32-token block), else the library's automatic choice, a pure
- * function of the arguments. Returns a negative value for unsupported
- * arguments.
+ * inside a 32-token block), or 0 for the balanced split chosen by
+ * `partition_tokens == 0` (see pa_decode). Returns a negative value for
+ * unsupported arguments.
  */
 int pa_decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int max_seq_len,
                                int partition_tokens);
@@ -121,10 +121,13 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  * in fp32 arithmetic on bf16 inputs, rounded to bf16 (nearest even).
  * A sequence with len_s == 0 gets zeros.
  *
- * Each sequence's tokens are split into partitions of
- * pa_decode_partition_tokens(...) tokens; partitions are processed in
- * parallel and their partial results merged with a log-sum-exp reduction
- * (the same value as unsplit attention, up to fp32 rounding). The call
+ * Split-KV: with partition_tokens > 0 every sequence's tokens are cut into
+ * partitions of that many tokens, processed in parallel. With
+ * partition_tokens == 0 (the default) the 16-token units of all (sequence,
+ * kv head) pairs, taken in order, are cut into equal contiguous shares, one
+ * per CTA, so every CTA streams the same number of bytes whatever the
+ * length mix. Either way partial results are merged with a log-sum-exp
+ * reduction (the same value as unsplit attention, up to fp32 rounding). The call
  * launches the decode kernel and, when some sequence may span more than one
  * partition, a merge kernel after it. Both are programmatic dependent
  * launches: they may start while the preceding kernel on the stream drains,
@@ -144,7 +147,8 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  *   head_dim           64 or 128
  *   block_size         8, 16 or 32
  *   scale              softmax scale (e.g. 1/sqrt(head_dim))
- *   partition_tokens   0 = automatic, else see pa_decode_partition_tokens
+ *   partition_tokens   0 = balanced split, else the partition length (see
+ *                      pa_decode_partition_tokens)
  *   max_seq_len        host-side upper bound of seq_lens (sizes the
  *                      workspace); longer sequences are clamped and flagged
  *   workspace          >= pa_decode_workspace_bytes(...) bytes, 256-B

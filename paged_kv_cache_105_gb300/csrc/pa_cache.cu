@@ -33,6 +33,9 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
     const int64_t th = r / chunks_per_row;  // token * n_kv + head
     const int h = (int)(th % n_kv);
     const int t = (int)(th / n_kv);
+    // both loads are issued before either is needed
+    const int64_t src = th * chunks_per_row + c;
+    const uint4 val = is_v ? __ldg(&v[src]) : __ldg(&k[src]);
     const int32_t slot = __ldg(&slot_mapping[t]);
     if (slot < 0) continue;  // padding
     if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
@@ -41,11 +44,7 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
     }
     const int64_t blk = slot / block_size, off = slot % block_size;
     const int64_t dst = ((blk * n_kv + h) * block_size + off) * chunks_per_row + c;
-    const int64_t src = th * chunks_per_row + c;
-    if (is_v)
-      v_pool[dst] = __ldg(&v[src]);
-    else
-      k_pool[dst] = __ldg(&k[src]);
+    (is_v ? v_pool : k_pool)[dst] = val;
   }
 }
 

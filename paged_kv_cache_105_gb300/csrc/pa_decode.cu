@@ -58,6 +58,15 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s: a wait that long is 
 constexpr uint64_t kWaitAfterFaultNs = 1000000ull;  // 1 ms once something has timed out
 constexpr int kMaxParts = 1024;
 constexpr int kMaxSeqs = 8192;
+constexpr int kMaxGrid = 1024;                      // persistent CTAs at most
+constexpr int kMinUnitsPerCta = 16;                 // balanced split: work per CTA at least
+#ifndef PA_PAIR_COST
+#define PA_PAIR_COST 16
+#endif
+// Balanced split: each (sequence, kv head) pair also costs this many units in
+// the stream being cut (its merge and bookkeeping), so a CTA whose share holds
+// many short pairs gets fewer units.
+constexpr int kPairCost = PA_PAIR_COST;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -65,12 +74,17 @@ struct DecodeArgs {
   const __nv_bfloat16* q;
   const int32_t* block_tables;
   const int32_t* seq_lens;
-  float* ws_o;               // [S][Hq][max_parts][D]  un-normalised partial outputs
-  float2* ws_ml;             // [S][Hq][max_parts]     (running max, sum) in log2 units
+  // Partials. Fixed partitions: [S][Hq][max_parts] rows. Balanced split:
+  // [kMaxGrid CTAs][2 slots][G heads] rows. O rows have D floats, (m, l) in
+  // log2 units.
+  float* ws_o;
+  float2* ws_ml;
   int32_t* work;             // [2]: items handed out dynamically, CTAs done
+  int4* pair_info;           // balanced: [S][Hkv] (first CTA, parts, first slot, -)
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
   int part_tokens, max_parts, len_cap;
+  int balanced;              // 1: even split of all units across CTAs
   int map3d;                 // 1: one TMA op loads both 64-column halves of a row
   float scale_log2;
 };
@@ -94,7 +108,7 @@ struct Cfg {
   static constexpr int NBARS = kWarps * STAGES + 4;  // stage barriers + mailbox
   static constexpr int MAIL_OFF = BAR_OFF + NBARS * 8;
   static constexpr int MISC_OFF = MAIL_OFF + 16;
-  static constexpr int FIN_OFF = MISC_OFF + 16;      // 2 x 16 floats
+  static constexpr int FIN_OFF = MISC_OFF + 32;      // 2 x 16 floats
   static constexpr int ML_OFF = FIN_OFF + 2 * 16 * 4;  // 3 warps x HEADS x (m, l)
   static constexpr int MERGE_OFF = ML_OFF + 3 * HEADS * 2 * 4;
   // Merge buffer: 3 warps x G heads x MSTRIDE floats; then the prefix table.
@@ -130,8 +144,15 @@ __device__ __forceinline__ float warp_sum_xor4(float v) {
   return v;
 }
 
-// Exclusive prefix over sequences of the item count n_kv * parts(len), and
-// the clamped lengths, both kept in shared memory for item lookups.
+// Balanced split: a pair's length in the stream (its units plus the pair cost;
+// an empty sequence takes no room).
+__device__ __forceinline__ int stream_len(int len) {
+  return len > 0 ? (len + kUnit - 1) / kUnit + kPairCost : 0;
+}
+
+// Exclusive prefix over sequences of the per-sequence count - items
+// n_kv * parts(len) for fixed partitions, 16-token units for the balanced
+// split - and the clamped lengths, both kept in shared memory.
 __device__ void build_prefix(int* prefix, int* lens, const DecodeArgs& a, int* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (a.num_seqs + kThreads - 1) / kThreads;
@@ -142,7 +163,7 @@ __device__ void build_prefix(int* prefix, int* lens, const DecodeArgs& a, int* w
     const int len = clamp_len(raw, a.len_cap);
     if (raw != len && blockIdx.x == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
     lens[s] = len;
-    sum += a.n_kv * parts_of(len, a.part_tokens);
+    sum += a.balanced ? stream_len(len) : a.n_kv * parts_of(len, a.part_tokens);
   }
   int incl = sum;
 #pragma unroll
@@ -157,7 +178,7 @@ __device__ void build_prefix(int* prefix, int* lens, const DecodeArgs& a, int* w
   int run = base + incl - sum;
   for (int s = b; s < e; ++s) {
     prefix[s] = run;
-    run += a.n_kv * parts_of(lens[s], a.part_tokens);
+    run += a.balanced ? stream_len(lens[s]) : a.n_kv * parts_of(lens[s], a.part_tokens);
   }
   if (tid == kThreads - 1) prefix[a.num_seqs] = base + incl;
 }
@@ -173,9 +194,16 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, cons
   }
 }
 
-// What a warp needs to know about one item.
+// A chunk of work: up to 128 units of one (sequence, kv head). `part` says
+// where the result goes (-1: the output itself; fixed partitions: the
+// partition index; balanced split: this CTA's partial slot 0 or 1). A
+// segment (one CTA's share of one (sequence, kv head)) may span several
+// chunks: the softmax state is reset at `first` and written at `last`.
 struct Item {
-  int s, g, p, nparts, tok_end, u_begin, n_units;
+  int s, g, tok_end, u_begin, n_units, part;
+  bool first, last;
+  bool holds_first;  // balanced split: the segment contains the pair's first unit
+  long long end;  // balanced split: unit position after this chunk
 };
 
 __device__ __forceinline__ Item decode_item(int item, const int* prefix, const int* lens,
@@ -187,16 +215,63 @@ __device__ __forceinline__ Item decode_item(int item, const int* prefix, const i
   }
   Item it;
   it.s = lo;
-  it.nparts = (prefix[lo + 1] - prefix[lo]) / a.n_kv;
+  const int nparts = (prefix[lo + 1] - prefix[lo]) / a.n_kv;
   const int local = item - prefix[lo];
-  it.g = local / it.nparts;
-  it.p = local - it.g * it.nparts;
+  it.g = local / nparts;
+  const int p = local - it.g * nparts;
   const int len = lens[lo];
-  const int tok_begin = it.p * a.part_tokens;
+  const int tok_begin = p * a.part_tokens;
   it.tok_end = min(len, tok_begin + a.part_tokens);
   it.u_begin = tok_begin / kUnit;
   it.n_units = it.tok_end > tok_begin ? (it.tok_end + kUnit - 1) / kUnit - it.u_begin : 0;
+  it.part = nparts == 1 ? -1 : p;
+  it.first = it.last = true;
+  it.holds_first = false;
+  it.end = 0;
   return it;
+}
+
+// Balanced split: the (sequence, kv head) pairs in order (sequence-major)
+// form one stream; pair (s, g) occupies [A, B) = kPairCost positions of
+// bookkeeping then its 16-token units [A + kPairCost, B). CTA c owns
+// positions [c W / n, (c+1) W / n) of the W-long stream. The chunk that
+// starts at or after position `pos` inside the CTA range [lo, hi): up to 128
+// units of one pair. Returns false if the range holds no more units.
+__device__ __forceinline__ bool decode_chunk(long long pos, long long lo, long long hi,
+                                             const int* prefix, const int* lens,
+                                             const DecodeArgs& a, Item& it) {
+#pragma unroll 1
+  while (pos < hi) {
+    int l = 0, h = a.num_seqs - 1;  // last sequence starting at or before pos
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if ((long long)a.n_kv * prefix[mid] <= pos) l = mid; else h = mid - 1;
+    }
+    const int w = prefix[l + 1] - prefix[l];  // > 0: empty sequences start nowhere
+    const long long base = (long long)a.n_kv * prefix[l];
+    const int g = (int)((pos - base) / w);
+    const long long A = base + (long long)g * w, B = A + w, R = A + kPairCost;
+    const long long seg_lo = R > lo ? R : lo, seg_hi = B < hi ? B : hi;
+    if (pos < seg_lo) pos = seg_lo;
+    if (pos >= seg_hi) {  // no units of this pair in the range: next pair
+      pos = B;
+      continue;
+    }
+    long long end = pos + kMaxUnitsPerPart;
+    if (end > seg_hi) end = seg_hi;
+    it.s = l;
+    it.g = g;
+    it.u_begin = (int)(pos - R);
+    it.n_units = (int)(end - pos);
+    it.tok_end = min(lens[l], (int)(end - R) * kUnit);
+    it.first = pos == seg_lo;
+    it.last = end == seg_hi;
+    it.part = (lo <= R && B <= hi) ? -1 : (lo >= A ? 0 : 1);
+    it.holds_first = seg_lo == R;
+    it.end = end == seg_hi ? B : end;  // where the next chunk search starts
+    return true;
+  }
+  return false;
 }
 
 __device__ __forceinline__ int units_of_warp(const Item& it, int warp) {
@@ -204,7 +279,8 @@ __device__ __forceinline__ int units_of_warp(const Item& it, int warp) {
 }
 
 // Lane j gets the pool blocks of this warp's j-th unit of the item (one per
-// TMA box; -1 = outside the pool, -2 = no tokens there).
+// TMA box), raw: they are checked where they are used, so that nothing
+// waits on these loads until the unit is issued.
 template <int BS, int BOXES, int ROWS>
 __device__ __forceinline__ void load_ids(int (&ids)[BOXES], const Item& it, int warp, int lane,
                                          const DecodeArgs& a) {
@@ -213,17 +289,20 @@ __device__ __forceinline__ void load_ids(int (&ids)[BOXES], const Item& it, int 
   const bool mine = lane < units_of_warp(it, warp);
 #pragma unroll
   for (int b = 0; b < BOXES; ++b) {
-    ids[b] = -2;
     const int tok = u * kUnit + b * ROWS;
-    if (mine && tok < it.tok_end) {
-      int id = __ldg(&table[tok / BS]);
-      if (id < 0 || id >= a.num_blocks) {
-        report(a.err, PA_DEV_ERR_BLOCK_ID);
-        id = -1;
-      }
-      ids[b] = id;
-    }
+    ids[b] = (mine && tok < it.tok_end) ? __ldg(&table[tok / BS]) : 0;
   }
+}
+
+// Valid-box mask of a unit: box b holds tokens (b * ROWS < nv) and its block
+// id lies inside the pool.
+template <int BOXES, int ROWS>
+__device__ __forceinline__ int box_mask(const int (&bid)[BOXES], int nv, int num_blocks) {
+  int mask = 0;
+#pragma unroll
+  for (int b = 0; b < BOXES; ++b)
+    if (b * ROWS < nv && bid[b] >= 0 && bid[b] < num_blocks) mask |= 1 << b;
+  return mask;
 }
 
 // B-operand fragments of the item's queries (head_dim x heads, column-major
@@ -306,27 +385,49 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   const int G = a.group;
   PA_EVENT(1);
 
-  // Items of this CTA: blockIdx.x, blockIdx.x + gridDim.x, then one per
-  // dynamic fetch (2 * gridDim.x + counter); the sequence only increases.
+  // Fixed partitions: this CTA's items are blockIdx.x, blockIdx.x +
+  // gridDim.x, then one per dynamic fetch (2 * gridDim.x + counter).
+  // Balanced split: the chunks of this CTA's unit range, in order.
   int item = blockIdx.x;
+  long long lo = 0, hi = 0, n_ctas = 1, U = 0;
   Item cur{}, nxt{};
   int ids_cur[BOXES], ids_nxt[BOXES];
   uint32_t qf_cur[NT][KS][2], qf_nxt[NT][KS][2];
-  bool have_cur = item < total;
-  bool have_nxt = false;
+  bool have_cur, have_nxt = false;
+  if (a.balanced) {
+    U = (long long)a.n_kv * total;  // stream length
+    n_ctas = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
+    if (n_ctas > gridDim.x) n_ctas = gridDim.x;
+    if (n_ctas < 1) n_ctas = 1;
+    // sequences with no tokens own no units: their outputs are zero
+    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
+      if (lens[sq] == 0)
+        for (int i = tid; i < a.n_q * D; i += kThreads)
+          a.out[(int64_t)sq * a.n_q * D + i] = __float2bfloat16_rn(0.f);
+    lo = (long long)blockIdx.x * U / n_ctas;
+    hi = (long long)(blockIdx.x + 1) * U / n_ctas;
+    have_cur = blockIdx.x < n_ctas && decode_chunk(lo, lo, hi, prefix, lens, a, cur);
+    if (have_cur) have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt);
+  } else {
+    have_cur = item < total;
+    if (have_cur) {
+      cur = decode_item(item, prefix, lens, a);
+      const int item1 = item + (int)gridDim.x;
+      have_nxt = item1 < total;
+      if (have_nxt) nxt = decode_item(item1, prefix, lens, a);
+    }
+  }
   if (have_cur) {
-    cur = decode_item(item, prefix, lens, a);
     load_ids<BS, BOXES, ROWS>(ids_cur, cur, warp, lane, a);
     load_q<D, NT>(qf_cur, cur, lane, a);
-    const int item1 = item + (int)gridDim.x;
-    have_nxt = item1 < total;
     if (have_nxt) {
-      nxt = decode_item(item1, prefix, lens, a);
       load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
       load_q<D, NT>(qf_nxt, nxt, lane, a);
     }
   }
 
+  float acc[NT][KS][4];               // this warp's softmax state for the segment
+  float mrun[NT][2], lrun[NT][2];
   uint32_t issued = 0, consumed = 0;  // units of this warp (same on all lanes)
   int issue_in_next = 0, issue_j = 0;  // issue cursor: (current or next item, unit)
 
@@ -352,9 +453,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       if (lane == 0) {
         const uint32_t st = issued % STAGES;
         const uint32_t fb = my_bar + 8 * st;
+        const int iu = (issue_in_next ? nxt.u_begin : cur.u_begin) + warp + issue_j * kWarps;
+        const int inv = min(kUnit, (issue_in_next ? nxt.tok_end : cur.tok_end) - iu * kUnit);
+        const int mask = box_mask<BOXES, ROWS>(bid, inv, a.num_blocks);
         int nload = 0;
 #pragma unroll
-        for (int b = 0; b < BOXES; ++b) nload += bid[b] >= 0;
+        for (int b = 0; b < BOXES; ++b) {
+          nload += mask >> b & 1;
+          if (b * ROWS < inv && !(mask >> b & 1)) report(a.err, PA_DEV_ERR_BLOCK_ID);
+        }
         if (nload == 0) {
           mbar_arrive(fb);
         } else {
@@ -363,7 +470,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
           const uint32_t vdst = kdst + C::KV_BYTES;
 #pragma unroll
           for (int b = 0; b < BOXES; ++b) {
-            if (bid[b] < 0) continue;
+            if (!(mask >> b & 1)) continue;
             // first row of this box: block row base plus the 16-token
             // window's offset inside a 32-token block
             const int tok_in_block = ((issue_in_next ? nxt.u_begin : cur.u_begin) +
@@ -393,19 +500,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     // ---- fetch item k + 2 of this CTA; the value is only needed after the
     // merge, so it is published then and its latency hides behind the units
     int fetched = INT_MAX;
-    if (tid == 0 && have_nxt) fetched = 2 * (int)gridDim.x + atomicAdd(&a.work[0], 1);
+    if (tid == 0 && have_nxt && !a.balanced)
+      fetched = 2 * (int)gridDim.x + atomicAdd(&a.work[0], 1);
 
-    // ---- stream this warp's units of the current item
-    float acc[NT][KS][4];
-    float mrun[NT][2], lrun[NT][2];
+    // ---- stream this warp's units of the current chunk
+    if (cur.first) {
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
+      for (int t = 0; t < NT; ++t) {
 #pragma unroll
-      for (int dt = 0; dt < KS; ++dt)
+        for (int dt = 0; dt < KS; ++dt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][dt][i] = 0.f;
-      mrun[t][0] = mrun[t][1] = -INFINITY;
-      lrun[t][0] = lrun[t][1] = 0.f;
+          for (int i = 0; i < 4; ++i) acc[t][dt][i] = 0.f;
+        mrun[t][0] = mrun[t][1] = -INFINITY;
+        lrun[t][0] = lrun[t][1] = 0.f;
+      }
     }
     const int n_mine = units_of_warp(cur, warp);
 #pragma unroll 1
@@ -413,11 +521,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       fill();
       const uint32_t st = consumed % STAGES;
       wait_or_flag(my_bar + 8 * st, (consumed / STAGES) & 1u, a, fault);
-      int mask = 0;
-#pragma unroll
-      for (int b = 0; b < BOXES; ++b)
-        mask |= (__shfl_sync(0xffffffffu, ids_cur[b], j) >= 0 ? 1 : 0) << b;
       const int nv = min(kUnit, cur.tok_end - (cur.u_begin + warp + j * kWarps) * kUnit);
+      int cbid[BOXES];
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b) cbid[b] = __shfl_sync(0xffffffffu, ids_cur[b], j);
+      const int mask = box_mask<BOXES, ROWS>(cbid, nv, a.num_blocks);
       const uint32_t kb = my_pipe + st * C::STAGE;
       const uint32_t vb = kb + C::KV_BYTES;
       bool all_ok = nv == kUnit;
@@ -509,11 +617,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     }
     fill();  // the next item's first units fly while the CTA merges
     PA_EVENT(3);
-    if (tid == 0) {
+    if (tid == 0 && !a.balanced) {
       mail[k & 3] = fetched;
       mbar_arrive(mail_bar + 8 * (k & 3));
     }
 
+    if (cur.last) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       lrun[t][0] = warp_sum_xor4(lrun[t][0]);
@@ -595,20 +704,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
     PA_EVENT(4);
     const int64_t row0 = (int64_t)cur.s * a.n_q + (int64_t)cur.g * G;
+    if (a.balanced && tid == 0 && cur.holds_first) {
+      // this CTA holds the pair's first unit: tell the merge where its parts are
+      const int w = prefix[cur.s + 1] - prefix[cur.s];
+      const long long B = (long long)a.n_kv * prefix[cur.s] + (long long)(cur.g + 1) * w;
+      const long long c1 = (B * n_ctas - 1) / U;
+      a.pair_info[(int64_t)cur.s * a.n_kv + cur.g] =
+          make_int4(blockIdx.x, (int)(c1 - blockIdx.x + 1), cur.part < 0 ? 0 : cur.part, 0);
+    }
     for (int i = tid; i < G * D; i += kThreads) {
       const int n = i / D, d = i - n * D;
       const float O = macc[n * C::MSTRIDE + d];
       const float M = fin[n], L = fin[16 + n];
-      if (cur.nparts == 1) {
+      if (cur.part < 0) {
         a.out[(row0 + n) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
       } else {
-        const int64_t wr = (row0 + n) * a.max_parts + cur.p;
+        const int64_t wr = a.balanced ? ((int64_t)blockIdx.x * 2 + cur.part) * G + n
+                                      : (row0 + n) * a.max_parts + cur.part;
         a.ws_o[wr * D + d] = O;
         if (d == 0) a.ws_ml[wr] = make_float2(M, L);
       }
     }
 
     __syncthreads();  // merge buffer, fin and misc are free again
+    }  // cur.last
     PA_EVENT(6);
 
     // ---- advance: the next item becomes current; learn the one after it
@@ -629,18 +748,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     } else {
       issue_j = 0;
     }
-    {
+    if (a.balanced) {
+      have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt);
+    } else {
       // the new next item is this CTA's item k + 2, fetched at the top of
       // this iteration into mailbox slot k mod 4
       const int slot = k & 3;
       wait_or_flag(mail_bar + 8 * slot, (k >> 2) & 1u, a, fault);
       const int item_n = mail[slot];
       have_nxt = item_n < total;
-      if (have_nxt) {
-        nxt = decode_item(item_n, prefix, lens, a);
-        load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
-        load_q<D, NT>(qf_nxt, nxt, lane, a);
-      }
+      if (have_nxt) nxt = decode_item(item_n, prefix, lens, a);
+    }
+    if (have_nxt) {
+      load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
+      load_q<D, NT>(qf_nxt, nxt, lane, a);
     }
   }
 
@@ -656,67 +777,101 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   }
 }
 
-// Merge of split-KV partitions: one warp per (sequence, query head) row with
-// more than one partition; lanes own head_dim columns. With m_p, l_p the
-// running max (log2 units) and sum of partition p and O_p its unnormalised
-// output: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
+// Merge of fixed split-KV partitions: one warp per (sequence, query head)
+// row with more than one partition; lanes own head_dim columns. With m_p,
+// l_p the running max (log2 units) and sum of partition p and O_p its
+// unnormalised output: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
+// M = max_p m_p. Fixed partitions: the parts of a row are its partitions.
+// Balanced split: the parts are the CTAs whose shares cut the row's
+// (sequence, kv head) pair, as recorded by the CTA holding its first unit.
 struct MergeArgs {
   __nv_bfloat16* out;
   const float* ws_o;
   const float2* ws_ml;
   const int32_t* seq_lens;
-  int num_seqs, n_q, part_tokens, max_parts, len_cap;
+  const int4* pair_info;
+  int num_seqs, n_q, n_kv, group, part_tokens, max_parts, len_cap, balanced;
 };
 
 constexpr int kMergeWarps = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs m) {
-  griddep_wait();  // the partitions come from the decode grid
+  griddep_wait();  // the partials come from the decode grid
   constexpr int PER = D / 32;
   const int lane = threadIdx.x & 31;
   const int rows = m.num_seqs * m.n_q;
   for (int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5); row < rows;
        row += gridDim.x * kMergeWarps) {
     const int s = row / m.n_q;
-    const int nparts = parts_of(clamp_len(__ldg(&m.seq_lens[s]), m.len_cap), m.part_tokens);
+    const int len = clamp_len(__ldg(&m.seq_lens[s]), m.len_cap);
+    int nparts;
+    long long rbase, rfirst, rstep;  // row of part q: q == 0 ? rfirst : rbase + q * rstep
+    if (m.balanced) {
+      // Balanced split: parts are CTAs c0 .. c0 + n - 1; CTA c keeps slot
+      // (2c + slot) * G + head; only c0 may use slot 1.
+      const int h = row - s * m.n_q, g = h / m.group, n = h - g * m.group;
+      const int4 pi = __ldcg(&m.pair_info[(int64_t)s * m.n_kv + g]);
+      nparts = len > 0 ? pi.y : 0;
+      rfirst = ((long long)pi.x * 2 + pi.z) * m.group + n;
+      rbase = (long long)pi.x * 2 * m.group + n;
+      rstep = 2LL * m.group;
+    } else {
+      nparts = parts_of(len, m.part_tokens);
+      rbase = rfirst = (long long)row * m.max_parts;
+      rstep = 1;
+    }
     if (nparts <= 1) continue;  // written directly by the decode kernel
-    const float2* ml = m.ws_ml + (int64_t)row * m.max_parts;
-    float M = -INFINITY;
-    for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&ml[q]).x);
+    auto rowq = [&](int q) -> long long { return q == 0 ? rfirst : rbase + q * rstep; };
+    // One round trip for the statistics (lane q holds part q) and the first
+    // kPre parts' rows; the rest stream in pairs.
+    constexpr int kPre = 4;
+    float2 st = make_float2(-INFINITY, 0.f);
+    if (lane < nparts) st = __ldcg(&m.ws_ml[rowq(lane)]);
+    float pre[kPre][PER];
+#pragma unroll
+    for (int q = 0; q < kPre; ++q)
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        pre[q][i] = q < nparts ? __ldcg(m.ws_o + rowq(q) * D + lane + 32 * i) : 0.f;
+    float M = st.x;
+    for (int q = lane + 32; q < nparts; q += 32) M = fmaxf(M, __ldcg(&m.ws_ml[rowq(q)]).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int q = lane; q < nparts; q += 32) {
-      const float2 v = __ldcg(&ml[q]);
+    const float wl = st.x == -INFINITY ? 0.f : fast_exp2(st.x - M);  // weight of part `lane`
+    float L = wl * st.y;
+    for (int q = lane + 32; q < nparts; q += 32) {
+      const float2 v = __ldcg(&m.ws_ml[rowq(q)]);
       L += v.x == -INFINITY ? 0.f : fast_exp2(v.x - M) * v.y;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float* op = m.ws_o + (int64_t)row * m.max_parts * D + lane;
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    int q = 0;
-    for (; q + 1 < nparts; q += 2) {
-      const float m0 = __ldcg(&ml[q]).x, m1 = __ldcg(&ml[q + 1]).x;
-      float o0[PER], o1[PER];
 #pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        o0[i] = __ldcg(op + (int64_t)q * D + 32 * i);
-        o1[i] = __ldcg(op + (int64_t)(q + 1) * D + 32 * i);
-      }
-      const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
-      const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+    for (int q = 0; q < kPre; ++q) {
+      const float w = __shfl_sync(0xffffffffu, wl, q);  // zero for q >= nparts
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += w0 * o0[i] + w1 * o1[i];
+      for (int i = 0; i < PER; ++i) acc[i] += w * pre[q][i];
     }
-    if (q < nparts) {
-      const float mq = __ldcg(&ml[q]).x;
-      const float w = mq == -INFINITY ? 0.f : fast_exp2(mq - M);
+    for (int q0 = kPre; q0 < nparts; q0 += kPre) {  // kPre parts in flight at a time
+      float mv[kPre], ov[kPre][PER];
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += w * __ldcg(op + (int64_t)q * D + 32 * i);
+      for (int q = 0; q < kPre; ++q) {
+        const bool in = q0 + q < nparts;
+        const long long r = rowq(in ? q0 + q : 0);
+        mv[q] = in ? __ldcg(&m.ws_ml[r]).x : -INFINITY;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) ov[q][i] = in ? __ldcg(m.ws_o + r * D + lane + 32 * i) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < kPre; ++q) {
+        const float w = mv[q] == -INFINITY ? 0.f : fast_exp2(mv[q] - M);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] += w * ov[q][i];
+      }
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i)
@@ -812,7 +967,8 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
     occ_for_smem[1] = occ;
   }
   int64_t grid = (int64_t)num_sms() * occ;
-  if (grid > items_upper) grid = items_upper;
+  if (!a.balanced && grid > items_upper) grid = items_upper;
+  if (grid > kMaxGrid) grid = kMaxGrid;
   if (grid < 1) grid = 1;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -826,12 +982,16 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_fail("pa_decode launch", e);
-  if (a.max_parts > 1) {
+  if (a.balanced || a.max_parts > 1) {
     MergeArgs m;
     m.out = a.out;
     m.ws_o = a.ws_o;
     m.ws_ml = a.ws_ml;
     m.seq_lens = a.seq_lens;
+    m.pair_info = a.pair_info;
+    m.n_kv = a.n_kv;
+    m.group = a.group;
+    m.balanced = a.balanced;
     m.num_seqs = a.num_seqs;
     m.n_q = a.n_q;
     m.part_tokens = a.part_tokens;
@@ -871,49 +1031,48 @@ static pa_status dispatch_bs(int bs, const DecodeArgs& a, const void* kp, const 
   }
 }
 
-// Partition size: explicit (a multiple of the 16-token unit, at most 2048),
-// or the largest of 512/256/128/64 tokens that still gives the persistent
-// grid (about 2 CTAs on each of ~150 SMs) several items each, estimating the
-// mean length as half the maximum.
+// Partition size: explicit (a multiple of the 16-token unit, at most 2048:
+// fixed partitions, dynamically scheduled), or 0 for the balanced split
+// (every CTA gets the same number of units of the whole batch).
 static int resolve_partition(int num_seqs, int n_kv, int block_size, int max_seq_len,
                              int partition_tokens) {
+  (void)num_seqs;
+  (void)n_kv;
   (void)block_size;
-  const int st = kUnit;
-  if (partition_tokens != 0) {
-    if (partition_tokens < st || partition_tokens % st != 0 ||
-        partition_tokens > kMaxUnitsPerPart * st)
-      return -1;
-    return partition_tokens;
-  }
-  const int64_t slots = 2 * 152;
-  const int64_t half = max_seq_len > 1 ? (max_seq_len + 1) / 2 : 1;
-  int P = 512;
-  while (P > 64) {
-    const int64_t items = (int64_t)num_seqs * n_kv * ((half + P - 1) / P);
-    if (items >= 4 * slots) break;
-    P >>= 1;
-  }
-  if (P < st) P = st;
-  return P;
+  (void)max_seq_len;
+  if (partition_tokens == 0) return 0;
+  if (partition_tokens < kUnit || partition_tokens % kUnit != 0 ||
+      partition_tokens > kMaxUnitsPerPart * kUnit)
+    return -1;
+  return partition_tokens;
 }
 
 struct WsLayout {
-  size_t o_off, ml_off, work_off, total;
+  size_t o_off, ml_off, work_off, tick_off, total;
   int max_parts;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static bool layout(int num_seqs, int n_q, int n_kv, int D, int P, int max_seq_len, WsLayout* w) {
-  const int64_t mp = max_seq_len <= 0 ? 1 : ((int64_t)max_seq_len + P - 1) / P;
-  if (mp > kMaxParts) return false;
-  w->max_parts = (int)mp;
-  const size_t rows = (size_t)num_seqs * n_q * mp;
+  size_t rows;
+  if (P == 0) {  // balanced split: two partial slots per CTA
+    w->max_parts = 0;
+    rows = (size_t)kMaxGrid * 2 * (n_q / n_kv);
+    // the unit stream must be addressable: num_seqs * units per sequence
+    if ((int64_t)num_seqs * (((int64_t)max_seq_len + kUnit - 1) / kUnit) >= ((int64_t)1 << 31))
+      return false;
+  } else {
+    const int64_t mp = max_seq_len <= 0 ? 1 : ((int64_t)max_seq_len + P - 1) / P;
+    if (mp > kMaxParts) return false;
+    w->max_parts = (int)mp;
+    rows = (size_t)num_seqs * n_q * mp;
+  }
   w->o_off = 0;
-  (void)n_kv;
   w->ml_off = align256(rows * D * sizeof(float));
   w->work_off = w->ml_off + align256(rows * sizeof(float2));
-  w->total = w->work_off + 256;
+  w->tick_off = w->work_off + 256;
+  w->total = w->tick_off + (P == 0 ? align256((size_t)num_seqs * n_kv * sizeof(int4)) : 0);
   return true;
 }
 
@@ -940,7 +1099,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_k
   if (!supported(head_dim, block_size, n_q_heads, n_kv_heads)) return 0;
   const int P =
       resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len, partition_tokens);
-  if (P <= 0) return 0;
+  if (P < 0) return 0;
   WsLayout w;
   if (!layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w)) return 0;
   return w.total;
@@ -963,7 +1122,7 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
   const int P = resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len,
                                   partition_tokens);
-  if (P <= 0) return PA_ERR_UNSUPPORTED;
+  if (P < 0) return PA_ERR_UNSUPPORTED;
   WsLayout w;
   if (!layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
     return PA_ERR_UNSUPPORTED;
@@ -984,6 +1143,8 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
   a.ws_ml = reinterpret_cast<float2*>(ws + w.ml_off);
   a.work = reinterpret_cast<int32_t*>(ws + w.work_off);
+  a.pair_info = reinterpret_cast<int4*>(ws + w.tick_off);
+  a.balanced = P == 0;
   a.err = err_word;
   a.num_seqs = num_seqs;
   a.max_blocks = max_blocks_per_seq;
@@ -996,7 +1157,7 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   a.len_cap = max_seq_len;
   a.scale_log2 = scale * kLog2e;
   a.map3d = 0;
-  const int64_t items_upper = (int64_t)num_seqs * n_kv_heads * w.max_parts;
+  const int64_t items_upper = (int64_t)num_seqs * n_kv_heads * (w.max_parts > 0 ? w.max_parts : 1);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 64) return dispatch_bs<64>(block_size, a, k_pool, v_pool, items_upper, st);
   return dispatch_bs<128>(block_size, a, k_pool, v_pool, items_upper, st);
@@ -1080,7 +1241,7 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_p
   const int P = resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len,
                                   partition_tokens);
   WsLayout w;
-  if (P <= 0 || !layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
+  if (P < 0 || !layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
     return PA_ERR_UNSUPPORTED;
   cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.work_off, 0,
                                   w.total - w.work_off, reinterpret_cast<cudaStream_t>(stream));

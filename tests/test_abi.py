@@ -55,8 +55,7 @@ def test_partition_choice(L):
     assert f(16, 8, 16, 32768, 128 * 16 + 16) < 0
     assert f(1, 1, 7, 10, 0) < 0                 # unsupported block size
     for args in [(256, 32, 16, 4096), (64, 8, 16, 2048), (5, 8, 16, 1900), (1, 1, 8, 1)]:
-        P = f(*args, 0)
-        assert P >= 16 and P % 16 == 0 and P <= 512
+        assert f(*args, 0) == 0                  # 0 selects the balanced split
 
 
 def test_workspace_bytes(L):
@@ -68,6 +67,11 @@ def test_workspace_bytes(L):
     assert f(16, 64, 7, 128, 16, 32768, 512) == 0     # heads not divisible
     assert f(16, 64, 2, 128, 16, 32768, 512) == 0     # group of 32 > 16
     assert f(1, 1, 1, 64, 16, 10**6, 64) == 0         # more than 1024 partitions
+    # balanced split: two partial slots per CTA (at most 1024 CTAs), whatever
+    # the longest sequence
+    b = f(16, 64, 8, 128, 16, 32768, 0)
+    assert b >= 1024 * 2 * 8 * (128 * 4 + 8)
+    assert b == f(16, 64, 8, 128, 16, 512, 0)
 
 
 # The two tests below pass fake addresses that host validation must reject

@@ -138,6 +138,28 @@ def test_workspace_reuse_is_deterministic():
         assert torch.equal(again.view(torch.int16), first.view(torch.int16))
 
 
+def test_balanced_split_workspace_reuse_is_deterministic():
+    wl = W.custom([50, 3000, 7, 1200, 4096, 0, 1], block_size=16, n_q_heads=32, n_kv_heads=8,
+                  head_dim=128, seed=16)
+    vals = on_dev(W.make_values(wl))
+    ws = B.decode_workspace(wl.num_seqs, 32, 8, 128, 16, wl.max_seq_len, 0, device=DEV)
+    first, err = gpu_step(wl, vals, partition_tokens=0, workspace=ws)
+    assert err == 0
+    for _ in range(3):
+        again, err = gpu_step(wl, vals, partition_tokens=0, workspace=ws, run_writes=False)
+        assert err == 0
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["balanced", "fixed"])
+def test_one_long_sequence_among_short_ones(mode):
+    # one sequence much longer than the rest: the balanced split cuts it across
+    # many CTAs; fixed partitions cut it into many partitions
+    lens = [4, 9, 31000, 3, 70, 1]
+    wl = W.custom(lens, block_size=16, n_q_heads=8, n_kv_heads=1, head_dim=128, seed=42)
+    full_parity(wl, partition_tokens=0 if mode == "balanced" else 256)
+
+
 def test_block_placement_does_not_matter():
     base = W.custom([900, 33, 1500], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128,
                     seed=21)
