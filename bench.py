@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--eager", action="store_true",
+                   help="launch every call from Python instead of replaying CUDA graphs")
     return p.parse_args()
 
 
@@ -299,22 +301,62 @@ def main():
                               wl.block_size, wl.max_seq_len, P, device=dev) for _ in reps]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     n_pairs = int(wl.cow_pairs.shape[0])
-    launches_per_step = 1 + (1 if n_pairs else 0) + (1 if wl.num_seqs else 0)
+    max_parts = 1 if P == 0 else -(-max(1, wl.max_seq_len) // P)
+    launches_per_step = ((1 if n_pairs else 0) + (1 if wl.num_seqs else 0)
+                         + (1 if wl.num_seqs else 0) + (1 if (P == 0 or max_parts > 1) else 0))
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
-        r = reps[i % replicas]
+    def calls_write(r):
         if n_pairs:
             B.pa_copy_blocks(r["k_pool"], r["v_pool"], t["pairs"], err_word=err)
         B.pa_reshape_and_cache(r["k_new"], r["v_new"], r["k_pool"], r["v_pool"], t["sm"],
                                err_word=err)
+
+    def calls_decode(j):
+        r = reps[j]
+        B.pa_decode(outs[j], r["q"], r["k_pool"], r["v_pool"], t["bt"], t["sl"],
+                    wl.scale, max_seq_len=wl.max_seq_len, workspace=wss[j],
+                    partition_tokens=P, err_word=err)
+
+    # Eager warm-up (also the library's one-time set-up), then, unless
+    # --eager, one CUDA graph per replica for the writes and one for the
+    # decode, as a serving engine replays its decode step.
+    for j in range(replicas):
+        calls_write(reps[j])
+        calls_decode(j)
+    torch.cuda.synchronize()
+    graphs = None
+    if not args.eager:
+        # per replica: the whole step (the decode is a programmatic dependent
+        # of the cache write, so their launches overlap) and the decode alone
+        graphs = []
+        cap = torch.cuda.Stream(dev)
+        for j in range(replicas):
+            gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs, stream=cap):
+                calls_write(reps[j])
+                calls_decode(j)
+            with torch.cuda.graph(gd, stream=cap):
+                calls_decode(j)
+            graphs.append((gs, gd))
+        torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        j = i % replicas
+        if graphs is not None:
+            graphs[j][0].replay()
+            return
+        calls_write(reps[j])
         if ev is not None:
             ev[0].record(stream)
-        B.pa_decode(outs[i % replicas], r["q"], r["k_pool"], r["v_pool"], t["bt"], t["sl"],
-                    wl.scale, max_seq_len=wl.max_seq_len, workspace=wss[i % replicas],
-                    partition_tokens=P, err_word=err)
+        calls_decode(j)
         if ev is not None:
             ev[1].record(stream)
+
+    def decode_only(i, ev):
+        ev[0].record(stream)
+        graphs[i % replicas][1].replay()
+        ev[1].record(stream)
 
     def barrier():
         if world > 1:
@@ -346,6 +388,11 @@ def main():
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
+    if graphs is not None:
+        # the decode kernel on its own, K launches, for the roofline
+        for k in range(args.steps):
+            decode_only(k, dec_ev[k])
+        torch.cuda.synchronize()
     # keep the load on a little past the timed region for the sampler
     t_post = time.perf_counter()
     while time.perf_counter() - t_post < 0.3:
@@ -434,6 +481,10 @@ def main():
                 "kernel": "decode_kernel (pa_decode)",
                 "peak_source": f"{peak_kind} hbm_gbs",
                 "alg_bytes_per_launch": alg_bytes,
+                "timing": ("CUDA events around each decode launch inside the timed steps"
+                           if args.eager else
+                           f"CUDA events around each of {args.steps} decode-graph replays "
+                           "right after the timed steps (same inputs, same replicas)"),
                 "decode_ms_avg": dec_avg_ms}
 
     cpu = None
@@ -469,6 +520,8 @@ def main():
                    "l2": f"inputs rotated over {replicas} replicas "
                          f"({replicas * kv_bytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2)",
                    "arithmetic": "bf16 operands, fp32 accumulation and softmax",
+                   "launch": "eager calls from Python" if args.eager else
+                             "one CUDA graph replay per step (copy, write, decode, merge)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_attended_per_s": tokens_per_s,
         "pct_of_peak": 100.0 * value / peak,

@@ -128,10 +128,15 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  * per CTA, so every CTA streams the same number of bytes whatever the
  * length mix. Either way partial results are merged with a log-sum-exp
  * reduction (the same value as unsplit attention, up to fp32 rounding). The call
- * launches the decode kernel and, when some sequence may span more than one
- * partition, a merge kernel after it. Both are programmatic dependent
- * launches: they may start while the preceding kernel on the stream drains,
- * and wait for it to complete before reading anything.
+ * launches the decode kernel and, when partials need merging, a merge kernel
+ * after it. Both are programmatic dependent launches. The decode kernel may
+ * start while the preceding kernel on the stream is still running if that
+ * kernel signals programmatic completion early (pa_reshape_and_cache does);
+ * it then reads q, block_tables and seq_lens right away, and waits for the
+ * preceding kernel to complete before it reads the pools or writes anything.
+ * So q, block_tables and seq_lens must not be written by a kernel that
+ * signals early and directly precedes pa_decode; kernels that do not use
+ * programmatic launch are always complete before pa_decode starts.
  *
  *   out                bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
  *   q                  bf16 [num_seqs][n_q_heads][head_dim], 16-B aligned
@@ -172,7 +177,10 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  * For token t with slot = slot_mapping[t] >= 0, every kv head h:
  *   k_pool[slot / block_size][h][slot % block_size][:] = k[t][h][:]
  *   v_pool[slot / block_size][h][slot % block_size][:] = v[t][h][:]
- * (bit copy). slot < 0 is padding and is skipped silently; slot >=
+ * (bit copy). The kernel signals programmatic completion as soon as it
+ * starts, so a following pa_decode may begin its set-up meanwhile (it waits
+ * for this kernel before reading the pools). slot < 0 is padding and is
+ * skipped silently; slot >=
  * num_blocks*block_size is skipped and flagged PA_DEV_ERR_SLOT. Two tokens
  * naming the same slot race (the caller must not do that).
  *

@@ -378,7 +378,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
-  griddep_wait();  // inputs may come from the previous kernel on the stream
+  // The prologue below reads only q, the tables and the lengths; under a
+  // programmatic launch it overlaps the preceding kernel (the cache write),
+  // and everything that touches the pools or the outputs waits for it.
   build_prefix(prefix, lens, a, reinterpret_cast<int*>(smem + C::ML_OFF));
   __syncthreads();
   const int total = prefix[a.num_seqs];
@@ -399,11 +401,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     n_ctas = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
     if (n_ctas > gridDim.x) n_ctas = gridDim.x;
     if (n_ctas < 1) n_ctas = 1;
-    // sequences with no tokens own no units: their outputs are zero
-    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
-      if (lens[sq] == 0)
-        for (int i = tid; i < a.n_q * D; i += kThreads)
-          a.out[(int64_t)sq * a.n_q * D + i] = __float2bfloat16_rn(0.f);
     lo = (long long)blockIdx.x * U / n_ctas;
     hi = (long long)(blockIdx.x + 1) * U / n_ctas;
     have_cur = blockIdx.x < n_ctas && decode_chunk(lo, lo, hi, prefix, lens, a, cur);
@@ -424,6 +421,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       load_ids<BS, BOXES, ROWS>(ids_nxt, nxt, warp, lane, a);
       load_q<D, NT>(qf_nxt, nxt, lane, a);
     }
+  }
+  griddep_wait();  // from here on: pool reads, output and workspace writes
+  if (a.balanced) {
+    // sequences with no tokens own no units: their outputs are zero
+    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
+      if (lens[sq] == 0)
+        for (int i = tid; i < a.n_q * D; i += kThreads)
+          a.out[(int64_t)sq * a.n_q * D + i] = __float2bfloat16_rn(0.f);
   }
 
   float acc[NT][KS][4];               // this warp's softmax state for the segment
@@ -899,8 +904,47 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // is `box_rows` rows of 64 columns (128 bytes, the swizzle span). For
 // D = 128 a 3-D view (64 columns, rows, 2 halves 128 bytes apart) lets one
 // copy fetch both halves of the rows; *map3d says which view was built.
+static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
+                                 int box_rows, bool try3d, int* map3d);
+
+// Encoding a tensor map costs host time on every call; a decode loop reuses
+// the same pools, so keep the last few per thread.
 static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
                                int box_rows, bool try3d, int* map3d) {
+  struct Entry {
+    const void* pool;
+    int D, box_rows, try3d, map3d;
+    int64_t rows;
+    CUtensorMap map;
+  };
+  static thread_local Entry cache[8];
+  static thread_local int used = 0, next = 0;
+  for (int i = 0; i < used; ++i) {
+    const Entry& e = cache[i];
+    if (e.pool == pool && e.D == D && e.rows == rows && e.box_rows == box_rows &&
+        e.try3d == (int)try3d) {
+      *map = e.map;
+      *map3d = e.map3d;
+      return PA_OK;
+    }
+  }
+  pa_status st = encode_pool_map(map, pool, D, rows, box_rows, try3d, map3d);
+  if (st != PA_OK) return st;
+  Entry& e = cache[next];
+  e.pool = pool;
+  e.D = D;
+  e.rows = rows;
+  e.box_rows = box_rows;
+  e.try3d = (int)try3d;
+  e.map3d = *map3d;
+  e.map = *map;
+  next = (next + 1) % 8;
+  if (used < 8) ++used;
+  return PA_OK;
+}
+
+static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
+                                 int box_rows, bool try3d, int* map3d) {
   auto fn = encode_fn();
   if (!fn) return cuda_fail_msg("pa_decode", "cuTensorMapEncodeTiled unavailable");
   if (try3d && D == 128) {
@@ -966,6 +1010,9 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
     occ_for_smem[0] = (int)smem;
     occ_for_smem[1] = occ;
   }
+#ifdef PA_MAX_CTAS_PER_SM
+  if (occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
+#endif
   int64_t grid = (int64_t)num_sms() * occ;
   if (!a.balanced && grid > items_upper) grid = items_upper;
   if (grid > kMaxGrid) grid = kMaxGrid;
