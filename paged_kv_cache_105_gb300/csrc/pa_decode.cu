@@ -58,10 +58,12 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s: a wait that long is 
 constexpr uint64_t kWaitAfterFaultNs = 1000000ull;  // 1 ms once something has timed out
 constexpr int kMaxParts = 1024;
 constexpr int kMaxSeqs = 8192;
-constexpr int kMaxGrid = 1024;                      // persistent CTAs at most
+constexpr int kMaxGrid = 512;                       // persistent CTAs at most
+constexpr int kMaxWorkers = kMaxGrid * 4;           // balanced split: one worker per warp
+constexpr int kMinUnitsPerWorker = 8;               // balanced split: work per warp at least
 constexpr int kMinUnitsPerCta = 16;                 // balanced split: work per CTA at least
 #ifndef PA_PAIR_COST
-#define PA_PAIR_COST 16
+#define PA_PAIR_COST 4
 #endif
 // Balanced split: each (sequence, kv head) pair also costs this many units in
 // the stream being cut (its merge and bookkeeping), so a CTA whose share holds
@@ -239,7 +241,8 @@ __device__ __forceinline__ Item decode_item(int item, const int* prefix, const i
 // units of one pair. Returns false if the range holds no more units.
 __device__ __forceinline__ bool decode_chunk(long long pos, long long lo, long long hi,
                                              const int* prefix, const int* lens,
-                                             const DecodeArgs& a, Item& it) {
+                                             const DecodeArgs& a, Item& it,
+                                             int max_units = kMaxUnitsPerPart) {
 #pragma unroll 1
   while (pos < hi) {
     int l = 0, h = a.num_seqs - 1;  // last sequence starting at or before pos
@@ -257,7 +260,7 @@ __device__ __forceinline__ bool decode_chunk(long long pos, long long lo, long l
       pos = B;
       continue;
     }
-    long long end = pos + kMaxUnitsPerPart;
+    long long end = pos + max_units;
     if (end > seg_hi) end = seg_hi;
     it.s = l;
     it.g = g;
@@ -324,6 +327,85 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Item
   }
 }
 
+// One 16-token unit of attention for the warp, online softmax in base 2.
+// K and V rows sit in shared memory (128-byte swizzled tiles, one box of
+// ROWS rows per block); tokens >= nv or in a box whose bit is clear in
+// `mask` are absent. S^T = K Q^T (tokens on M, the query heads of the group
+// on N), then O^T += V^T P^T, with P^T made from the score fragment by
+// movmatrix.
+template <int D, int ROWS, int NT>
+__device__ __forceinline__ void attend_unit(uint32_t kb, uint32_t vb, int lane, int nv, int mask,
+                                            float scale_log2,
+                                            const uint32_t (&qf)[NT][D / 16][2],
+                                            float (&acc)[NT][D / 16][4], float (&mrun)[NT][2],
+                                            float (&lrun)[NT][2]) {
+  constexpr int KS = D / 16;
+  constexpr int BOX_BYTES = (D / 64) * ROWS * 128;
+    // ---- S^T = K Q^T for 16 tokens x 8 heads (per n-tile)
+    float sc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+    {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t row = kb + (r / ROWS) * BOX_BYTES + (r % ROWS) * 128;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int h = ks >> 2;
+        const int c = ((ks & 3) << 1) + (lane >> 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          mma_bf16_16816(sc[t], a0, a1, a2, a3, qf[t][ks][0], qf[t][ks][1]);
+      }
+    }
+    // ---- mask, online softmax (base 2), P^T fragments
+    const int tA = lane >> 2, tB = tA + 8;
+    const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
+    const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float pv[4];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const float xa = okA ? sc[t][jj] * scale_log2 : -INFINITY;
+        const float xb = okB ? sc[t][jj + 2] * scale_log2 : -INFINITY;
+        const float mx = warp_max_xor4(fmaxf(xa, xb));
+        const float m_new = fmaxf(mrun[t][jj], mx);
+        const float base = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(mrun[t][jj] - base);
+        pv[jj] = fast_exp2(xa - base);
+        pv[jj + 2] = fast_exp2(xb - base);
+        lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
+        mrun[t][jj] = m_new;
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+          acc[t][dt][jj] *= alpha;
+          acc[t][dt][jj + 2] *= alpha;
+        }
+      }
+      pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
+      pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
+    }
+    // ---- O^T += V^T P^T
+    {
+      const int mi = lane >> 3;
+      const int r = (lane & 7) + (mi >> 1) * 8;
+      const uint32_t row = vb + (r / ROWS) * BOX_BYTES + (r % ROWS) * 128;
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt) {
+        const int h = dt >> 2;
+        const int c = ((dt & 3) << 1) + (mi & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+      }
+    }
+}
+
 #ifdef PA_TRACE
 // Per-CTA event log for timing studies: [cta][slot] = (event << 56) | ns.
 constexpr int kTraceSlots = 256;
@@ -338,9 +420,24 @@ __device__ int g_trace_n[1024];
             ((uint64_t)(ev) << 56) | (globaltimer_ns() & ((1ull << 56) - 1));     \
     }                                                                             \
   } while (0)
+// Per-warp log for the balanced-split kernel: [worker][slot].
+__device__ uint64_t g_wtrace[2048 * 16];
+__device__ int g_wtrace_n[2048];
+#define PA_WEVENT(w, ev)                                                          \
+  do {                                                                            \
+    if ((threadIdx.x & 31) == 0 && (w) < 2048) {                                  \
+      const int i_ = g_wtrace_n[w]++;                                             \
+      if (i_ < 16)                                                                \
+        g_wtrace[(w) * 16 + i_] =                                                 \
+            ((uint64_t)(ev) << 56) | (globaltimer_ns() & ((1ull << 56) - 1));     \
+    }                                                                             \
+  } while (0)
 #else
 #define PA_EVENT(ev) \
   do {               \
+  } while (0)
+#define PA_WEVENT(w, ev) \
+  do {                   \
   } while (0)
 #endif
 
@@ -551,69 +648,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         __syncwarp();
       }
 
-      // ---- S^T = K Q^T for 16 tokens x 8 heads (per n-tile)
-      float sc[NT][4];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-      {
-        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const uint32_t row = kb + (r / ROWS) * C::BOX_BYTES + (r % ROWS) * 128;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int h = ks >> 2;
-          const int c = ((ks & 3) << 1) + (lane >> 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-            mma_bf16_16816(sc[t], a0, a1, a2, a3, qf_cur[t][ks][0], qf_cur[t][ks][1]);
-        }
-      }
-      // ---- mask, online softmax (base 2), P^T fragments
-      const int tA = lane >> 2, tB = tA + 8;
-      const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
-      const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
-      uint32_t pb[NT][2];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float pv[4];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const float xa = okA ? sc[t][jj] * a.scale_log2 : -INFINITY;
-          const float xb = okB ? sc[t][jj + 2] * a.scale_log2 : -INFINITY;
-          const float mx = warp_max_xor4(fmaxf(xa, xb));
-          const float m_new = fmaxf(mrun[t][jj], mx);
-          const float base = m_new == -INFINITY ? 0.f : m_new;
-          const float alpha = fast_exp2(mrun[t][jj] - base);
-          pv[jj] = fast_exp2(xa - base);
-          pv[jj + 2] = fast_exp2(xb - base);
-          lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
-          mrun[t][jj] = m_new;
-#pragma unroll
-          for (int dt = 0; dt < KS; ++dt) {
-            acc[t][dt][jj] *= alpha;
-            acc[t][dt][jj + 2] *= alpha;
-          }
-        }
-        pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
-        pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
-      }
-      // ---- O^T += V^T P^T
-      {
-        const int mi = lane >> 3;
-        const int r = (lane & 7) + (mi >> 1) * 8;
-        const uint32_t row = vb + (r / ROWS) * C::BOX_BYTES + (r % ROWS) * 128;
-#pragma unroll
-        for (int dt = 0; dt < KS; ++dt) {
-          const int h = dt >> 2;
-          const int c = ((dt & 3) << 1) + (mi & 1);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-            mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
-        }
-      }
+      attend_unit<D, ROWS, NT>(kb, vb, lane, nv, mask, a.scale_log2, qf_cur, acc, mrun, lrun);
       // The stage is refilled by this warp's next fill(); generic writes to
       // it (the zeroed rows) must be ordered before that TMA.
       if (!all_ok) fence_proxy_async_smem();
@@ -780,6 +815,296 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       atomicExch(&a.work[1], 0);
     }
   }
+}
+
+#ifndef PA_SPLIT_BUDGET
+#define PA_SPLIT_BUDGET 16384
+#endif
+
+// Shared-memory layout of the balanced-split kernel: per-warp stage rings,
+// their mbarriers, a fault flag, then the prefix and length tables.
+template <int D, int BS, int NT>
+struct SplitCfg {
+  using C = Cfg<D, BS, NT>;
+  static constexpr int STAGE = C::STAGE;
+  static constexpr int STAGES_RAW = PA_SPLIT_BUDGET / STAGE;
+  static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
+  static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
+  static constexpr int MISC_OFF = BAR_OFF + kWarps * STAGES * 8;
+  static constexpr int PREFIX_OFF = MISC_OFF + 64;  // [0..15] ints: fault flag, scan scratch
+  static size_t smem_bytes(int num_seqs) {
+    return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(2 * num_seqs + 1);
+  }
+};
+
+// Balanced split at warp granularity: every warp is a worker that owns an
+// equal contiguous share of the unit stream (see decode_chunk) and streams
+// it alone through its own stage ring, writing each pair it completes
+// straight from its registers (or, for a pair cut at its share's edges, one
+// of its two partial slots). No barrier and no cross-warp merge in the main
+// loop; the merge kernel combines the cut pairs.
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(kThreads)
+split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+             const DecodeArgs a) {
+  using C = Cfg<D, BS, NT>;
+  using SC = SplitCfg<D, BS, NT>;
+  constexpr int ROWS = C::ROWS, BOXES = C::BOXES, KH = C::KH, STAGES = SC::STAGES;
+  constexpr int KS = C::KS;
+  constexpr int kChunk = 32;  // units per chunk: one table entry per lane
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  int* misc = reinterpret_cast<int*>(smem + SC::MISC_OFF);
+  int* prefix = reinterpret_cast<int*>(smem + SC::PREFIX_OFF);
+  int* lens = prefix + a.num_seqs + 1;
+  volatile int* fault = misc;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t my_pipe = sbase + warp * STAGES * SC::STAGE;
+  const uint32_t my_bar = sbase + SC::BAR_OFF + warp * STAGES * 8;
+
+  if (tid == 0) {
+    for (int i = 0; i < kWarps * STAGES; ++i) mbar_init(sbase + SC::BAR_OFF + 8 * i, 1);
+    misc[0] = 0;
+    fence_mbarrier_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  build_prefix(prefix, lens, a, misc + 8);
+  __syncthreads();
+  const int G = a.group;
+  const long long U = (long long)a.n_kv * prefix[a.num_seqs];  // stream length
+  long long n_workers = (U + kMinUnitsPerWorker - 1) / kMinUnitsPerWorker;
+  if (n_workers > (long long)gridDim.x * kWarps) n_workers = (long long)gridDim.x * kWarps;
+  if (n_workers < 1) n_workers = 1;
+  const long long worker = (long long)blockIdx.x * kWarps + warp;
+  const long long lo = worker * U / n_workers, hi = (worker + 1) * U / n_workers;
+
+  Item cur{}, nxt{};
+  int ids_cur[BOXES], ids_nxt[BOXES];
+  uint32_t qf_cur[NT][KS][2], qf_nxt[NT][KS][2];
+  bool have_cur = worker < n_workers && decode_chunk(lo, lo, hi, prefix, lens, a, cur, kChunk);
+  bool have_nxt = have_cur && decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt, kChunk);
+
+  // lane j: the pool blocks of unit j of the chunk (raw; checked where used)
+  auto load_ids_w = [&](int (&ids)[BOXES], const Item& it) {
+    const int32_t* table = a.block_tables + (int64_t)it.s * a.max_blocks;
+#pragma unroll
+    for (int b = 0; b < BOXES; ++b) {
+      const int tok = (it.u_begin + lane) * kUnit + b * ROWS;
+      ids[b] = (lane < it.n_units && tok < it.tok_end) ? __ldg(&table[tok / BS]) : 0;
+    }
+  };
+  if (have_cur) {
+    load_ids_w(ids_cur, cur);
+    load_q<D, NT>(qf_cur, cur, lane, a);
+    if (have_nxt) {
+      load_ids_w(ids_nxt, nxt);
+      load_q<D, NT>(qf_nxt, nxt, lane, a);
+    }
+  }
+  PA_WEVENT(worker, 1);
+  griddep_wait();  // from here on: pool reads, output and workspace writes
+  // sequences with no tokens own no units: their outputs are zero
+  for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
+    if (lens[sq] == 0)
+      for (int i = tid; i < a.n_q * D; i += kThreads)
+        a.out[(int64_t)sq * a.n_q * D + i] = __float2bfloat16_rn(0.f);
+
+  float acc[NT][KS][4];
+  float mrun[NT][2], lrun[NT][2];
+  uint32_t issued = 0, consumed = 0;
+  int issue_in_next = 0, issue_j = 0;
+
+  auto fill = [&]() {
+#pragma unroll 1
+    while (issued - consumed < (uint32_t)STAGES) {
+      const int nm = issue_in_next ? nxt.n_units : cur.n_units;
+      if (issue_j >= nm) {
+        if (!issue_in_next && have_nxt) {
+          issue_in_next = 1;
+          issue_j = 0;
+          continue;
+        }
+        break;
+      }
+      int bid[BOXES];
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b)
+        bid[b] = __shfl_sync(0xffffffffu, issue_in_next ? ids_nxt[b] : ids_cur[b], issue_j);
+      if (lane == 0) {
+        const Item& it = issue_in_next ? nxt : cur;
+        const uint32_t st = issued % STAGES;
+        const uint32_t fb = my_bar + 8 * st;
+        const int iu = it.u_begin + issue_j;
+        const int inv = min(kUnit, it.tok_end - iu * kUnit);
+        const int mask = box_mask<BOXES, ROWS>(bid, inv, a.num_blocks);
+        int nload = 0;
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b) {
+          nload += mask >> b & 1;
+          if (b * ROWS < inv && !(mask >> b & 1)) report(a.err, PA_DEV_ERR_BLOCK_ID);
+        }
+        if (nload == 0) {
+          mbar_arrive(fb);
+        } else {
+          mbar_arrive_expect_tx(fb, (uint32_t)nload * 2 * C::BOX_BYTES);
+          const uint32_t kdst = my_pipe + st * SC::STAGE;
+          const uint32_t vdst = kdst + C::KV_BYTES;
+#pragma unroll
+          for (int b = 0; b < BOXES; ++b) {
+            if (!(mask >> b & 1)) continue;
+            const int tok_in_block = (iu * kUnit) % BS + b * ROWS;
+            const int32_t y = (bid[b] * a.n_kv + it.g) * BS + (BS > kUnit ? tok_in_block : 0);
+            if (KH == 2 && a.map3d) {
+              tma_load_3d(kdst + b * C::BOX_BYTES, &tmk, 0, y, 0, fb);
+              tma_load_3d(vdst + b * C::BOX_BYTES, &tmv, 0, y, 0, fb);
+            } else {
+#pragma unroll
+              for (int h = 0; h < KH; ++h) {
+                tma_load_2d(kdst + b * C::BOX_BYTES + h * ROWS * 128, &tmk, h * 64, y, fb);
+                tma_load_2d(vdst + b * C::BOX_BYTES + h * ROWS * 128, &tmv, h * 64, y, fb);
+              }
+            }
+          }
+        }
+      }
+      ++issued;
+      ++issue_j;
+    }
+  };
+
+#pragma unroll 1
+  while (have_cur) {
+    if (cur.first) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[t][dt][i] = 0.f;
+        mrun[t][0] = mrun[t][1] = -INFINITY;
+        lrun[t][0] = lrun[t][1] = 0.f;
+      }
+    }
+#pragma unroll 1
+    for (int j = 0; j < cur.n_units; ++j) {
+      fill();
+      const uint32_t st = consumed % STAGES;
+      wait_or_flag(my_bar + 8 * st, (consumed / STAGES) & 1u, a, fault);
+      if (consumed == 0) PA_WEVENT(worker, 2);  // first data
+      const int nv = min(kUnit, cur.tok_end - (cur.u_begin + j) * kUnit);
+      int cbid[BOXES];
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b) cbid[b] = __shfl_sync(0xffffffffu, ids_cur[b], j);
+      const int mask = box_mask<BOXES, ROWS>(cbid, nv, a.num_blocks);
+      const uint32_t kb = my_pipe + st * SC::STAGE;
+      const uint32_t vb = kb + C::KV_BYTES;
+      bool all_ok = nv == kUnit;
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b)
+        if (b * ROWS < nv && !(mask >> b & 1)) all_ok = false;
+      if (!all_ok) {
+        // Rows of absent tokens may hold anything (even NaN): zero their V
+        // so that a zero weight times the row stays zero.
+        uint8_t* vgen = smem + (vb - sbase);
+        for (int i = lane; i < kUnit * KH * 8; i += 32) {
+          const int r = i / (KH * 8), rest = i % (KH * 8);
+          const int h = rest / 8, c = rest % 8;
+          if (r >= nv || !(mask >> (r / ROWS) & 1))
+            *reinterpret_cast<uint4*>(vgen + (r / ROWS) * C::BOX_BYTES + h * ROWS * 128 +
+                                      (r % ROWS) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      attend_unit<D, ROWS, NT>(kb, vb, lane, nv, mask, a.scale_log2, qf_cur, acc, mrun, lrun);
+      // The stage is refilled by this warp's next fill(); generic writes to
+      // it (the zeroed rows) must be ordered before that TMA.
+      if (!all_ok) fence_proxy_async_smem();
+      __syncwarp();
+      ++consumed;
+    }
+    fill();  // keep the ring full across the write below
+
+    if (cur.last) {
+      PA_WEVENT(worker, 3);  // a segment's units done
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        lrun[t][0] = warp_sum_xor4(lrun[t][0]);
+        lrun[t][1] = warp_sum_xor4(lrun[t][1]);
+      }
+      const int64_t row0 = (int64_t)cur.s * a.n_q + (int64_t)cur.g * G;
+      const long long prow = (worker * 2 + (cur.part < 0 ? 0 : cur.part)) * G;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int n = t * 8 + 2 * (lane & 3) + (i & 1);
+          if (n >= G) continue;
+          const float l = lrun[t][i & 1];
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+          for (int dt = 0; dt < KS; ++dt) {
+            const int d = dt * 16 + (lane >> 2) + 8 * (i >> 1);
+            if (cur.part < 0)
+              a.out[(row0 + n) * D + d] = __float2bfloat16_rn(acc[t][dt][i] * inv);
+            else
+              a.ws_o[(prow + n) * D + d] = acc[t][dt][i];
+          }
+        }
+        if (cur.part >= 0 && lane < 4) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int n = t * 8 + 2 * lane + jj;
+            if (n < G) a.ws_ml[prow + n] = make_float2(mrun[t][jj], lrun[t][jj]);
+          }
+        }
+      }
+      if (lane == 0 && cur.holds_first) {
+        // this worker holds the pair's first unit: tell the merge where its parts are
+        const int w = prefix[cur.s + 1] - prefix[cur.s];
+        const long long B = (long long)a.n_kv * prefix[cur.s] + (long long)(cur.g + 1) * w;
+        const long long c1 = (B * n_workers - 1) / U;
+        a.pair_info[(int64_t)cur.s * a.n_kv + cur.g] =
+            make_int4((int)worker, (int)(c1 - worker + 1), cur.part < 0 ? 0 : cur.part, 0);
+      }
+    }
+
+    // ---- advance
+    have_cur = have_nxt;
+    if (!have_cur) break;
+    cur = nxt;
+#pragma unroll
+    for (int b = 0; b < BOXES; ++b) ids_cur[b] = ids_nxt[b];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf_cur[t][ks][0] = qf_nxt[t][ks][0];
+        qf_cur[t][ks][1] = qf_nxt[t][ks][1];
+      }
+    if (issue_in_next) issue_in_next = 0; else issue_j = 0;
+    have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt, kChunk);
+    if (have_nxt) {
+      load_ids_w(ids_nxt, nxt);
+      load_q<D, NT>(qf_nxt, nxt, lane, a);
+    }
+  }
+
+  PA_WEVENT(worker, 4);
+#ifdef PA_TRACE
+  {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    if (lane == 0 && worker < 2048 && g_wtrace_n[worker] < 16)
+      g_wtrace[worker * 16 + g_wtrace_n[worker]++] = (5ull << 56) | smid;
+  }
+#endif
+  __syncthreads();
+  griddep_launch_dependents();  // the merge may start launching
 }
 
 // Merge of fixed split-KV partitions: one warp per (sequence, query head)
@@ -991,25 +1316,35 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   }
   a.map3d = k3 && v3;
 
-  const size_t smem = C::smem_bytes(a.num_seqs, a.group);
-  static int configured = 0;  // largest dynamic smem size already allowed
-  static int occ_for_smem[2] = {-1, 0};
-  if ((int)smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return cuda_fail("pa_decode smem attribute", e);
-    configured = (int)smem;
-  }
-  int occ = 0;
-  if (occ_for_smem[0] == (int)smem) {
-    occ = occ_for_smem[1];
-  } else {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  // Allow the dynamic shared memory and find the CTAs per SM, once per
+  // (kernel, size).
+  auto prepare = [](auto fn, size_t smem, int* configured, int* occ_cache, int* occ) {
+    if ((int)smem > *configured) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return cuda_fail("pa_decode smem attribute", e);
+      *configured = (int)smem;
+    }
+    if (occ_cache[0] == (int)smem) {
+      *occ = occ_cache[1];
+      return PA_OK;
+    }
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fn, kThreads, smem);
     if (e != cudaSuccess) return cuda_fail("pa_decode occupancy", e);
-    if (occ < 1) return cuda_fail_msg("pa_decode", "kernel does not fit on an SM");
-    occ_for_smem[0] = (int)smem;
-    occ_for_smem[1] = occ;
-  }
+    if (*occ < 1) return cuda_fail_msg("pa_decode", "kernel does not fit on an SM");
+    occ_cache[0] = (int)smem;
+    occ_cache[1] = *occ;
+    return PA_OK;
+  };
+  static int cfg_item = 0, cfg_split = 0;
+  static int occ_item[2] = {-1, 0}, occ_split[2] = {-1, 0};
+  auto skern = split_kernel<D, BS, NT>;
+  const size_t smem = a.balanced ? SplitCfg<D, BS, NT>::smem_bytes(a.num_seqs)
+                                 : C::smem_bytes(a.num_seqs, a.group);
+  int occ = 0;
+  st = a.balanced ? prepare(skern, smem, &cfg_split, occ_split, &occ)
+                  : prepare(kern, smem, &cfg_item, occ_item, &occ);
+  if (st != PA_OK) return st;
 #ifdef PA_MAX_CTAS_PER_SM
   if (occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
 #endif
@@ -1027,7 +1362,8 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
+  cudaError_t e = a.balanced ? cudaLaunchKernelEx(&cfg, skern, tmk, tmv, a)
+                              : cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_fail("pa_decode launch", e);
   if (a.balanced || a.max_parts > 1) {
     MergeArgs m;
@@ -1103,9 +1439,9 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static bool layout(int num_seqs, int n_q, int n_kv, int D, int P, int max_seq_len, WsLayout* w) {
   size_t rows;
-  if (P == 0) {  // balanced split: two partial slots per CTA
+  if (P == 0) {  // balanced split: two partial slots per worker (warp)
     w->max_parts = 0;
-    rows = (size_t)kMaxGrid * 2 * (n_q / n_kv);
+    rows = (size_t)kMaxWorkers * 2 * (n_q / n_kv);
     // the unit stream must be addressable: num_seqs * units per sequence
     if ((int64_t)num_seqs * (((int64_t)max_seq_len + kUnit - 1) / kUnit) >= ((int64_t)1 << 31))
       return false;
@@ -1255,9 +1591,18 @@ extern "C" int pa_trace_read(uint64_t* host, int* counts) {
   if (cudaMemcpyFromSymbol(host, pa::g_trace, sizeof(pa::g_trace)) != cudaSuccess) return -1;
   if (cudaMemcpyFromSymbol(counts, pa::g_trace_n, sizeof(pa::g_trace_n)) != cudaSuccess)
     return -1;
-  static int zeros[1024] = {0};
-  if (cudaMemcpyToSymbol(pa::g_trace_n, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  static int zeros[2048] = {0};
+  if (cudaMemcpyToSymbol(pa::g_trace_n, zeros, sizeof(pa::g_trace_n)) != cudaSuccess) return -1;
   return pa::kTraceSlots;
+}
+
+extern "C" int pa_wtrace_read(uint64_t* host, int* counts) {
+  if (cudaMemcpyFromSymbol(host, pa::g_wtrace, sizeof(pa::g_wtrace)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(counts, pa::g_wtrace_n, sizeof(pa::g_wtrace_n)) != cudaSuccess)
+    return -1;
+  static int zeros[2048] = {0};
+  if (cudaMemcpyToSymbol(pa::g_wtrace_n, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  return 16;
 }
 #endif
 
