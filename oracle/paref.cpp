@@ -350,3 +350,121 @@ extern "C" int paref_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32
   }
   return skipped;
 }
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 (OCP FP8 formats): sign, 4 exponent bits with bias 7, 3 mantissa
+// bits. Exponent field 0 is subnormal (value m * 2^-9); the all-ones
+// exponent with all-ones mantissa is NaN; there is no infinity, so the
+// largest finite value is 1.75 * 2^8 = 448.
+// ---------------------------------------------------------------------------
+
+extern "C" double paref_e4m3_decode(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  double mag = e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+// Round a non-negative double to the nearest integer, ties to even.
+static double round_half_even(double v) {
+  double f = std::floor(v);
+  double diff = v - f;
+  if (diff > 0.5) return f + 1.0;
+  if (diff < 0.5) return f;
+  return std::fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+extern "C" uint8_t paref_e4m3_encode(double x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  double a = std::fabs(x);
+  if (a >= 448.0) return sign | 0x7E;  // saturate
+  if (a < std::ldexp(1.0, -6)) {
+    // subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest normal
+    const int m = (int)round_half_even(std::ldexp(a, 9));
+    return sign | (uint8_t)m;  // m == 8 encodes exponent 1, mantissa 0
+  }
+  int e = (int)std::floor(std::log2(a));
+  if (std::ldexp(1.0, e) > a) --e;        // guard log2 rounding
+  if (std::ldexp(1.0, e + 1) <= a) ++e;
+  int m = (int)round_half_even((std::ldexp(a, -e) - 1.0) * 8.0);
+  if (m == 8) {
+    m = 0;
+    ++e;
+  }
+  if (e > 8 || (e == 8 && m == 7)) return sign | 0x7E;  // rounded past 448
+  return sign | (uint8_t)(((e + 7) << 3) | m);
+}
+
+extern "C" int paref_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v, uint8_t* k_pool,
+                                           uint8_t* v_pool, const int32_t* slot_mapping,
+                                           int num_tokens, int num_blocks, int n_kv_heads,
+                                           int head_dim, int block_size, float k_scale,
+                                           float v_scale) {
+  int skipped = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int32_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
+      ++skipped;
+      continue;
+    }
+    const int32_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < n_kv_heads; ++h) {
+      const int64_t dst = (((int64_t)blk * n_kv_heads + h) * block_size + off) * head_dim;
+      const int64_t src = ((int64_t)t * n_kv_heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) {
+        const float kq = (float)bf16_to_double(k[src + d]) / k_scale;  // fp32 division
+        const float vq = (float)bf16_to_double(v[src + d]) / v_scale;
+        k_pool[dst + d] = paref_e4m3_encode(kq);
+        v_pool[dst + d] = paref_e4m3_encode(vq);
+      }
+    }
+  }
+  return skipped;
+}
+
+extern "C" int paref_attention_paged_fp8(double* out, const uint16_t* q, const uint8_t* k_pool,
+                                         const uint8_t* v_pool, const int32_t* block_tables,
+                                         const int32_t* seq_lens, int num_seqs, int max_blocks,
+                                         int num_blocks, int n_q_heads, int n_kv_heads,
+                                         int head_dim, int block_size, double scale,
+                                         double k_scale, double v_scale, const int32_t* rows,
+                                         int n_rows) {
+  if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -1;
+  const int group = n_q_heads / n_kv_heads;
+  const int total = rows ? n_rows : num_seqs * n_q_heads;
+  for (int r = 0; r < total; ++r) {
+    const int s = rows ? rows[2 * r] : r / n_q_heads;
+    const int h = rows ? rows[2 * r + 1] : r % n_q_heads;
+    if (s < 0 || s >= num_seqs || h < 0 || h >= n_q_heads) return -1;
+    const int len = seq_lens[s];
+    if (len < 0 || (int64_t)len > (int64_t)max_blocks * block_size) return -1;
+    const int g = h / group;
+    double* o = out + (int64_t)r * head_dim;
+    for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+    if (len == 0) continue;
+    const uint16_t* qr = q + ((int64_t)s * n_q_heads + h) * head_dim;
+    std::vector<double> x(len);
+    std::vector<int64_t> off(len);
+    for (int i = 0; i < len; ++i) {
+      const int32_t phys = block_tables[(int64_t)s * max_blocks + i / block_size];
+      if (phys < 0 || phys >= num_blocks) return -1;
+      off[i] = (((int64_t)phys * n_kv_heads + g) * block_size + i % block_size) * head_dim;
+      double dot = 0.0;
+      for (int d = 0; d < head_dim; ++d)
+        dot += bf16_to_double(qr[d]) * (paref_e4m3_decode(k_pool[off[i] + d]) * k_scale);
+      x[i] = scale * dot;
+    }
+    double m = x[0];
+    for (int i = 1; i < len; ++i) m = x[i] > m ? x[i] : m;
+    double denom = 0.0;
+    for (int i = 0; i < len; ++i) denom += std::exp(x[i] - m);
+    for (int i = 0; i < len; ++i) {
+      const double w = std::exp(x[i] - m) / denom;
+      for (int d = 0; d < head_dim; ++d)
+        o[d] += w * (paref_e4m3_decode(v_pool[off[i] + d]) * v_scale);
+    }
+  }
+  return 0;
+}

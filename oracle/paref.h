@@ -125,6 +125,34 @@ int paref_reshape_and_cache(const uint16_t* k, const uint16_t* v, uint16_t* k_po
 int paref_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* pairs, int n_pairs,
                       int n_kv_heads, int head_dim, int block_size, int num_blocks);
 
+/* ---------------- FP8 KV cache ("PagedAttention" (mlapandio.dev), Cons and
+   honest limits, and "Serving: vLLM and PagedAttention" section 3.1: an fp8
+   KV cache halves the cache and the bytes read per step). The format is
+   OCP FP8 E4M3 (bias 7, no infinities, 0x7F/0xFF = NaN, max 448); a stored
+   code times a per-tensor fp32 scale gives the value. ------------------- */
+
+/* Value of an E4M3 code (NaN for 0x7F / 0xFF). */
+double paref_e4m3_decode(uint8_t code);
+/* E4M3 code nearest to x (ties to even), saturating to +-448; NaN -> 0x7F. */
+uint8_t paref_e4m3_encode(double x);
+
+/* Cache write into fp8 pools: code = e4m3(fp32(k) / k_scale), the division
+   in fp32 (round to nearest), likewise for v. Pools are uint8
+   [num_blocks][n_kv_heads][block_size][head_dim]. Returns skipped slots. */
+int paref_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v, uint8_t* k_pool,
+                                uint8_t* v_pool, const int32_t* slot_mapping, int num_tokens,
+                                int num_blocks, int n_kv_heads, int head_dim, int block_size,
+                                float k_scale, float v_scale);
+
+/* paref_attention_paged over fp8 pools: K_i = decode(k code) * k_scale,
+   V_i = decode(v code) * v_scale, in fp64. */
+int paref_attention_paged_fp8(double* out, const uint16_t* q, const uint8_t* k_pool,
+                              const uint8_t* v_pool, const int32_t* block_tables,
+                              const int32_t* seq_lens, int num_seqs, int max_blocks,
+                              int num_blocks, int n_q_heads, int n_kv_heads, int head_dim,
+                              int block_size, double scale, double k_scale, double v_scale,
+                              const int32_t* rows, int n_rows);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,7 @@ _lock = threading.Lock()
 
 i32p = C.POINTER(C.c_int32)
 u16p = C.POINTER(C.c_uint16)
+u8p = C.POINTER(C.c_uint8)
 f64p = C.POINTER(C.c_double)
 
 
@@ -58,6 +59,15 @@ def lib():
                                                       C.c_int, C.c_int, C.c_int, C.c_int]),
                 "paref_copy_blocks": (C.c_int, [u16p, u16p, i32p, C.c_int, C.c_int, C.c_int,
                                                 C.c_int, C.c_int]),
+                "paref_e4m3_decode": (C.c_double, [C.c_uint8]),
+                "paref_e4m3_encode": (C.c_uint8, [C.c_double]),
+                "paref_reshape_and_cache_fp8": (C.c_int, [u16p, u16p, u8p, u8p, i32p, C.c_int,
+                                                          C.c_int, C.c_int, C.c_int, C.c_int,
+                                                          C.c_float, C.c_float]),
+                "paref_attention_paged_fp8": (C.c_int, [f64p, u16p, u8p, u8p, i32p, i32p,
+                                                        C.c_int, C.c_int, C.c_int, C.c_int,
+                                                        C.c_int, C.c_int, C.c_int, C.c_double,
+                                                        C.c_double, C.c_double, i32p, C.c_int]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -265,3 +275,60 @@ def copy_blocks(k_pool, v_pool, pairs) -> int:
     pr, prp = _i32(np.asarray(pairs).reshape(-1, 2))
     NB, Hkv, bs, d = k_pool.shape
     return lib().paref_copy_blocks(kpp, vpp, prp, pr.shape[0], Hkv, d, bs, NB)
+
+
+# ----------------------------------------------------------------- fp8 (E4M3)
+
+def e4m3_decode(code: int) -> float:
+    return lib().paref_e4m3_decode(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    return lib().paref_e4m3_encode(float(x))
+
+
+def _u8(a):
+    a = np.asarray(a)
+    if a.dtype != np.uint8 or not a.flags["C_CONTIGUOUS"]:
+        raise TypeError("fp8 pools must be C-contiguous uint8 arrays")
+    return a, a.ctypes.data_as(u8p)
+
+
+def reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale) -> int:
+    """In place on the uint8 pools: E4M3 codes of fp32(k) / k_scale."""
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    k_pool, kpp = _u8(k_pool)
+    v_pool, vpp = _u8(v_pool)
+    sm, smp = _i32(slot_mapping)
+    T, Hkv, d = k.shape
+    NB, Hkv2, bs, d2 = k_pool.shape
+    assert Hkv2 == Hkv and d2 == d and sm.shape == (T,)
+    return lib().paref_reshape_and_cache_fp8(kp, vp, kpp, vpp, smp, T, NB, Hkv, d, bs,
+                                             float(k_scale), float(v_scale))
+
+
+def attention_paged_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale, k_scale, v_scale,
+                        rows=None):
+    """fp64 paged attention over E4M3 pools (uint8 codes times the scales)."""
+    q, qp = _u16(q)
+    k_pool, kp = _u8(k_pool)
+    v_pool, vp = _u8(v_pool)
+    bt, btp = _i32(block_tables)
+    sl, slp = _i32(seq_lens)
+    S, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_pool.shape
+    assert d2 == d and v_pool.shape == k_pool.shape
+    if rows is None:
+        out = np.zeros((S, Hq, d), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        r, rp = _i32(np.asarray(rows).reshape(-1, 2))
+        nr = r.shape[0]
+        out = np.zeros((nr, d), dtype=np.float64)
+    rc = lib().paref_attention_paged_fp8(out.ctypes.data_as(f64p), qp, kp, vp, btp, slp, S,
+                                         bt.shape[1], NB, Hq, Hkv, d, bs, float(scale),
+                                         float(k_scale), float(v_scale), rp, nr)
+    if rc != 0:
+        raise ValueError("oracle fp8 attention: invalid block table, length or shape")
+    return out
