@@ -217,6 +217,71 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n
                          int32_t* err_word, pa_stream_t stream);
 
 /*
+ * FP8 KV cache. "PagedAttention" (mlapandio.dev), "Cons and honest limits",
+ * and "Serving: vLLM and PagedAttention", section 3.1, name an fp8 KV cache
+ * as the way to halve the cache (and with it the bytes every decode step
+ * reads). The pages fix no format; these calls use OCP FP8 E4M3 (bias 7, no
+ * infinities, codes 0x7F/0xFF are NaN, largest finite value 448) with one
+ * fp32 scale per tensor: a stored code c stands for e4m3(c) * scale.
+ * Pools are uint8 [num_blocks][n_kv_heads][block_size][head_dim], one byte
+ * per element, otherwise laid out like the bf16 pools.
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 — pa_reshape_and_cache into fp8 pools.
+ * For token t with slot >= 0 and every kv head h and column d:
+ *   k_pool[slot / bs][h][slot % bs][d] = E4M3(fp32(k[t][h][d]) / k_scale)
+ * (the division rounded to nearest in fp32; the conversion rounded to
+ * nearest even and saturated to +-448; NaN gives a NaN code), likewise v
+ * with v_scale. Padding, range checks, flags and the early completion
+ * signal are those of pa_reshape_and_cache.
+ *
+ *   k, v              bf16 [num_tokens][n_kv_heads][head_dim], 16-B aligned
+ *   k_pool, v_pool    uint8 pools, 16-B aligned
+ *   head_dim          64 or 128; block_size 8, 16 or 32
+ *   k_scale, v_scale  finite, > 0 (else PA_ERR_INVALID_ARG)
+ */
+pa_status pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
+                                   const int32_t* slot_mapping, int num_tokens, int num_blocks,
+                                   int n_kv_heads, int head_dim, int block_size, float k_scale,
+                                   float v_scale, int32_t* err_word, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks_fp8 — pa_copy_blocks on uint8 (fp8) pools: block
+ * pairs[p][1] becomes a bit copy of block pairs[p][0] in both pools.
+ * Arguments, checks and flags as pa_copy_blocks.
+ */
+pa_status pa_copy_blocks_fp8(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs,
+                             int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                             int32_t* err_word, pa_stream_t stream);
+
+/*
+ * pa_decode_fp8 — pa_decode over fp8 pools. For each (sequence, query head)
+ * the result is attention with
+ *   K_i = e4m3(k code) * k_scale,  V_i = e4m3(v code) * v_scale
+ * and the softmax scale `scale`, exactly as pa_decode defines it otherwise.
+ * Always the balanced split (no partition argument); the workspace is that
+ * of pa_decode_workspace_bytes(num_seqs, n_q_heads, n_kv_heads, 128,
+ * block_size, max_seq_len, 0), with the same zeroing rule.
+ *
+ * Arithmetic: codes are exact in f16; q is rounded from bf16 to f16 (exact
+ * for |q| in [2^-14, 65504]; smaller values lose low bits, larger ones are
+ * out of range) and the scores and the weighted sum of V are f16 tensor-core
+ * products with fp32 accumulation; softmax in fp32.
+ *
+ *   k_pool, v_pool    uint8 pools, 16-B aligned
+ *   head_dim          128 only (else PA_ERR_UNSUPPORTED)
+ *   k_scale, v_scale  finite, > 0 (else PA_ERR_INVALID_ARG)
+ *   everything else   as pa_decode
+ */
+pa_status pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                        int max_blocks_per_seq, int num_blocks, int n_q_heads, int n_kv_heads,
+                        int head_dim, int block_size, float scale, float k_scale, float v_scale,
+                        int max_seq_len, void* workspace, size_t workspace_bytes,
+                        int32_t* err_word, pa_stream_t stream);
+
+/*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device
  * memory. The paper has no counterpart; this is a library convenience.
  *

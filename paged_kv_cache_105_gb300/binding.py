@@ -40,6 +40,11 @@ SIGNATURES = {
     "pa_copy_blocks": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "pa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                C.c_float, _i, _i, _vp, _vp]),
+    "pa_reshape_and_cache_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, C.c_float,
+                                      C.c_float, _vp, _vp]),
+    "pa_copy_blocks_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
+                           C.c_float, C.c_float, _i, _vp, C.c_size_t, _vp, _vp]),
 }
 
 # Size of the library's fixed scratch used by pa_decode_noalloc (64 MiB).
@@ -227,4 +232,79 @@ def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, *, 
                                  int(max_seq_len), _ptr(err_word), _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_decode_noalloc", st)
+    return out
+
+
+# ------------------------------------------------------------ fp8 (E4M3) cache
+# Pools are uint8 tensors of E4M3 codes; a code times the tensor's scale is
+# the value (include/pa.h, "FP8 KV cache").
+
+def pa_reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale, *,
+                             err_word=None, stream=None):
+    """k_pool[slot // bs, :, slot % bs] = E4M3(fp32(k[t]) / k_scale) (and v)."""
+    dev = k.device
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.uint8, 4, dev)
+    _check(v_pool, "v_pool", torch.uint8, 4, dev)
+    _check(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    T, Hkv, D = k.shape
+    NB, Hkv2, bs, D2 = k_pool.shape
+    if v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch between new K/V and the pools")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    st = lib().pa_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool),
+                                        _ptr(slot_mapping), T, NB, Hkv, D, bs, float(k_scale),
+                                        float(v_scale), _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_reshape_and_cache_fp8", st)
+
+
+def pa_copy_blocks_fp8(k_pool, v_pool, pairs, *, err_word=None, stream=None):
+    """Block pairs[p, 1] of both uint8 pools becomes a copy of block pairs[p, 0]."""
+    dev = k_pool.device
+    _check(k_pool, "k_pool", torch.uint8, 4)
+    _check(v_pool, "v_pool", torch.uint8, 4, dev)
+    _check(pairs, "pairs", torch.int32, 2, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    NB, Hkv, bs, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or (pairs.numel() and pairs.shape[1] != 2):
+        raise ValueError("pools must match and pairs must be [n, 2]")
+    st = lib().pa_copy_blocks_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), pairs.shape[0], Hkv,
+                                  D, bs, NB, _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_copy_blocks_fp8", st)
+
+
+def pa_decode_fp8(out, q, k_pool, v_pool, block_tables, seq_lens, scale, k_scale, v_scale, *,
+                  max_seq_len, workspace, err_word=None, stream=None):
+    """pa_decode over E4M3 pools: K = code * k_scale, V = code * v_scale.
+    The workspace is decode_workspace(..., partition_tokens=0)."""
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.uint8, 4, dev)
+    _check(v_pool, "v_pool", torch.uint8, 4, dev)
+    _check(block_tables, "block_tables", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _check(workspace, "workspace", torch.uint8, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    if tuple(out.shape) != (S, Hq, D) or D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens must have one row per sequence")
+    st = lib().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                             _ptr(seq_lens), S, block_tables.shape[1], NB, Hq, Hkv, D, bs,
+                             float(scale), float(k_scale), float(v_scale), int(max_seq_len),
+                             _ptr(workspace), workspace.numel(), _ptr(err_word),
+                             _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_decode_fp8", st)
     return out

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -71,6 +73,55 @@ copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
   }
 }
 
+// fp8 cache write: one thread per 16 codes (16 bytes of output, 32 bytes of
+// bf16 input) of one (token, kv head) row of K or V. code = E4M3 of
+// fp32(x) / scale, the division rounded to nearest, the conversion rounded
+// to nearest even and saturated to +-448.
+__global__ void __launch_bounds__(256)
+reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                             const int32_t* __restrict__ slot_mapping, int num_tokens,
+                             int num_blocks, int n_kv, int chunks_per_row, int block_size,
+                             float k_scale, float v_scale, int32_t* err) {
+  griddep_launch_dependents();
+  const int64_t per_tensor = (int64_t)num_tokens * n_kv * chunks_per_row;
+  const int64_t total = 2 * per_tensor;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per_tensor;
+    const int64_t r = is_v ? i - per_tensor : i;
+    const int c = (int)(r % chunks_per_row);
+    const int64_t th = r / chunks_per_row;  // token * n_kv + head
+    const int h = (int)(th % n_kv);
+    const int t = (int)(th / n_kv);
+    const int64_t src = 2 * (th * chunks_per_row + c);  // two 16-byte bf16 chunks
+    const uint4* in = is_v ? v : k;
+    const uint4 x0 = __ldg(&in[src]), x1 = __ldg(&in[src + 1]);
+    const int32_t slot = __ldg(&slot_mapping[t]);
+    if (slot < 0) continue;
+    if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
+      if (c == 0 && h == 0 && !is_v) report(err, PA_DEV_ERR_SLOT);
+      continue;
+    }
+    const float sc = is_v ? v_scale : k_scale;
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // two bf16 words = 4 values -> 4 codes (one 32-bit word)
+      const uint32_t a = w[2 * j], b = w[2 * j + 1];
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(a << 16), sc),
+                                          __fdiv_rn(__uint_as_float(a & 0xffff0000u), sc));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(b << 16), sc),
+                                          __fdiv_rn(__uint_as_float(b & 0xffff0000u), sc));
+      o[j] = lo | (hi << 16);
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    const int64_t dst = ((blk * n_kv + h) * block_size + off) * chunks_per_row + c;
+    (is_v ? v_pool : k_pool)[dst] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 static bool supported_dims(int head_dim, int block_size) {
   return (head_dim == 64 || head_dim == 128) &&
          (block_size == 8 || block_size == 16 || block_size == 32);
@@ -124,4 +175,54 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* p
       (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks launch", e);
+}
+
+extern "C" pa_status pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool,
+                                              void* v_pool, const int32_t* slot_mapping,
+                                              int num_tokens, int num_blocks, int n_kv_heads,
+                                              int head_dim, int block_size, float k_scale,
+                                              float v_scale, int32_t* err_word,
+                                              pa_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || n_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (!supported_dims(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (!(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+    return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_blocks * n_kv_heads * block_size >= (int64_t)1 << 31)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_pool || !v_pool || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PA_ERR_INVALID_ARG;
+  const int chunks = head_dim / 16;  // 16 codes per output chunk
+  const int64_t total = 2LL * num_tokens * n_kv_heads * chunks;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  reshape_and_cache_fp8_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+      (const uint4*)k, (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping,
+      num_tokens, num_blocks, n_kv_heads, chunks, block_size, k_scale, v_scale, err_word);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_reshape_and_cache_fp8 launch", e);
+}
+
+extern "C" pa_status pa_copy_blocks_fp8(void* k_pool, void* v_pool, const int32_t* pairs,
+                                        int n_pairs, int n_kv_heads, int head_dim,
+                                        int block_size, int num_blocks, int32_t* err_word,
+                                        pa_stream_t stream) {
+  if (n_pairs < 0 || num_blocks <= 0 || n_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (!supported_dims(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (n_pairs > 65535) return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!k_pool || !v_pool || !pairs) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_INVALID_ARG;
+  const int64_t chunks = (int64_t)n_kv_heads * block_size * head_dim / 16;  // 1-byte codes
+  const int threads = 256;
+  int64_t bx = (2 * chunks + threads - 1) / threads;
+  if (bx > 64) bx = 64;
+  dim3 grid((unsigned)bx, (unsigned)n_pairs);
+  copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
+      (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks_fp8 launch", e);
 }

@@ -88,14 +88,17 @@ struct DecodeArgs {
   int part_tokens, max_parts, len_cap;
   int balanced;              // 1: even split of all units across CTAs
   int map3d;                 // 1: one TMA op loads both 64-column halves of a row
-  float scale_log2;
+  float scale_log2;          // softmax scale (times the K scale for fp8) times log2(e)
+  float v_scale;             // fp8: the V scale; 1 for bf16
 };
 
-template <int D, int BS, int NT>
+// EB: bytes per cached element (2: bf16, 1: fp8 E4M3).
+template <int D, int BS, int NT, int EB = 2>
 struct Cfg {
   static constexpr int ROWS = BS < kUnit ? BS : kUnit;  // rows per TMA box
   static constexpr int BOXES = kUnit / ROWS;            // boxes (blocks) per unit
-  static constexpr int KH = D / 64;                     // 128-byte halves of a row
+  static constexpr int KH = D * EB / 128;               // 128-byte pieces of a row
+  static_assert(KH >= 1, "a cached row must span at least one 128-byte swizzle span");
   static constexpr int BOX_BYTES = KH * ROWS * 128;     // one box of K (or V), all halves
   static constexpr int KV_BYTES = BOXES * BOX_BYTES;    // K (or V) of a unit = 16 * D * 2
   static constexpr int STAGE = 2 * KV_BYTES;
@@ -404,6 +407,132 @@ __device__ __forceinline__ void attend_unit(uint32_t kb, uint32_t vb, int lane, 
           mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
       }
     }
+}
+
+// ------------------------------------------------------------ fp8 (E4M3) K/V
+//
+// The fp8 cache holds E4M3 codes; a code times the tensor's fp32 scale is the
+// value. Codes are exact in f16, so the contractions run as f16 mma.sync on
+// the codes (scores S = codes . q, the K scale folded into the softmax scale;
+// the V scale applied to the output). A row of D = 128 codes is one 128-byte
+// swizzle span. ldmatrix on byte data gives each lane 4 consecutive codes of
+// one row per 8x8 b16 matrix; that fixes the order in which the k (and, for
+// V^T, the m) index of a 16-wide slice is walked:
+//   K (A of S^T = K Q^T): lane (g, c) holds d = 4c .. 4c+3 of a 16-column
+//     chunk; k-slots (2c, 2c+1) take d (4c, 4c+1) and (2c+8, 2c+9) take
+//     d (4c+2, 4c+3). Q (the B operand) is loaded in the same order.
+//   V (A of O^T += V^T P^T): the codes of 8 tokens x 16 d, converted, are two
+//     8x8 f16 matrices M1 (d = 4j'+{0,1}) and M2 (d = 4j'+{2,3}); movmatrix
+//     transposes each into the (d, token) layout, so rows 0-7 of a 16-row
+//     A tile are the d of M1 and rows 8-15 those of M2 (see fp8_out_d).
+
+// B-operand fragments of the query heads in f16, k-slots in the order above.
+template <int D, int NT>
+__device__ __forceinline__ void load_q_f16(uint32_t (&qf)[NT][D / 16][2], const Item& it,
+                                           int lane, const DecodeArgs& a) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int n = t * 8 + (lane >> 2);
+    const bool real = n < a.group;
+    const uint2* qrow = reinterpret_cast<const uint2*>(
+        a.q + ((int64_t)it.s * a.n_q + (int64_t)it.g * a.group + (real ? n : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint2 v = real ? __ldg(&qrow[ks * 4 + (lane & 3)]) : make_uint2(0u, 0u);
+      // bf16 -> f32 is a shift; f32 -> f16 rounds to nearest
+      qf[t][ks][0] = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+      qf[t][ks][1] = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    }
+  }
+}
+
+// Head-dim column of accumulator row `r` (0..15) of 16-column chunk dt.
+__device__ __forceinline__ int fp8_out_d(int dt, int r) {
+  const int j = r & 7;
+  return dt * 16 + 4 * (j >> 1) + (j & 1) + (r >> 3) * 2;
+}
+
+// attend_unit over fp8 codes: one 16-token unit, 128-byte rows.
+template <int D, int ROWS, int NT>
+__device__ __forceinline__ void attend_unit_fp8(uint32_t kb, uint32_t vb, int lane, int nv,
+                                                int mask, float scale_log2,
+                                                const uint32_t (&qf)[NT][D / 16][2],
+                                                float (&acc)[NT][D / 16][4],
+                                                float (&mrun)[NT][2], float (&lrun)[NT][2]) {
+  constexpr int KS = D / 16;
+  constexpr int BOX_BYTES = ROWS * 128;
+  static_assert(D == 128, "fp8 rows are one 128-byte span");
+  // lanes 8i..8i+7 address matrix i: tokens (i & 1) * 8 + 0..7 of chunk 2p + (i >> 1)
+  const int mi = lane >> 3;
+  const int r = (lane & 7) + (mi & 1) * 8;
+  const int rsw = r & 7;
+  const uint32_t roff = (r / ROWS) * BOX_BYTES + (r % ROWS) * 128;
+  // ---- S^T = K Q^T
+  float sc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+  for (int p = 0; p < KS / 2; ++p) {
+    const int c = 2 * p + (mi >> 1);
+    uint32_t x[4];
+    ldsm_x4(kb + roff + ((c ^ rsw) << 4), x[0], x[1], x[2], x[3]);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16x2x2(x[2 * hf], a0, a2);      // token g
+      e4m3x4_to_f16x2x2(x[2 * hf + 1], a1, a3);  // token g + 8
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        mma_f16_16816(sc[t], a0, a1, a2, a3, qf[t][2 * p + hf][0], qf[t][2 * p + hf][1]);
+    }
+  }
+  // ---- mask, online softmax (base 2), P^T fragments
+  const int tA = lane >> 2, tB = tA + 8;
+  const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
+  const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
+  uint32_t pb[NT][2];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float pv[4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const float xa = okA ? sc[t][jj] * scale_log2 : -INFINITY;
+      const float xb = okB ? sc[t][jj + 2] * scale_log2 : -INFINITY;
+      const float mx = warp_max_xor4(fmaxf(xa, xb));
+      const float m_new = fmaxf(mrun[t][jj], mx);
+      const float base = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = fast_exp2(mrun[t][jj] - base);
+      pv[jj] = fast_exp2(xa - base);
+      pv[jj + 2] = fast_exp2(xb - base);
+      lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
+      mrun[t][jj] = m_new;
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt) {
+        acc[t][dt][jj] *= alpha;
+        acc[t][dt][jj + 2] *= alpha;
+      }
+    }
+    pb[t][0] = movmatrix_trans(pack_f16x2(pv[0], pv[1]));
+    pb[t][1] = movmatrix_trans(pack_f16x2(pv[2], pv[3]));
+  }
+  // ---- O^T += V^T P^T
+#pragma unroll
+  for (int p = 0; p < KS / 2; ++p) {
+    const int c = 2 * p + (mi >> 1);
+    uint32_t y[4];
+    ldsm_x4(vb + roff + ((c ^ rsw) << 4), y[0], y[1], y[2], y[3]);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t m1a, m2a, m1b, m2b;
+      e4m3x4_to_f16x2x2(y[2 * hf], m1a, m2a);      // tokens 0-7
+      e4m3x4_to_f16x2x2(y[2 * hf + 1], m1b, m2b);  // tokens 8-15
+      const uint32_t a0 = movmatrix_trans(m1a), a1 = movmatrix_trans(m2a);
+      const uint32_t a2 = movmatrix_trans(m1b), a3 = movmatrix_trans(m2b);
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        mma_f16_16816(acc[t][2 * p + hf], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+    }
+  }
 }
 
 #ifdef PA_TRACE
@@ -823,9 +952,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
 // Shared-memory layout of the balanced-split kernel: per-warp stage rings,
 // their mbarriers, a fault flag, then the prefix and length tables.
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool FP8 = false>
 struct SplitCfg {
-  using C = Cfg<D, BS, NT>;
+  using C = Cfg<D, BS, NT, FP8 ? 1 : 2>;
   static constexpr int STAGE = C::STAGE;
   static constexpr int STAGES_RAW = PA_SPLIT_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
@@ -842,13 +971,14 @@ struct SplitCfg {
 // it alone through its own stage ring, writing each pair it completes
 // straight from its registers (or, for a pair cut at its share's edges, one
 // of its two partial slots). No barrier and no cross-warp merge in the main
-// loop; the merge kernel combines the cut pairs.
-template <int D, int BS, int NT>
+// loop; the merge kernel combines the cut pairs. FP8: the pools hold E4M3
+// codes (attend_unit_fp8).
+template <int D, int BS, int NT, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads)
 split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
              const DecodeArgs a) {
-  using C = Cfg<D, BS, NT>;
-  using SC = SplitCfg<D, BS, NT>;
+  using C = Cfg<D, BS, NT, FP8 ? 1 : 2>;
+  using SC = SplitCfg<D, BS, NT, FP8>;
   constexpr int ROWS = C::ROWS, BOXES = C::BOXES, KH = C::KH, STAGES = SC::STAGES;
   constexpr int KS = C::KS;
   constexpr int kChunk = 32;  // units per chunk: one table entry per lane
@@ -898,12 +1028,16 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       ids[b] = (lane < it.n_units && tok < it.tok_end) ? __ldg(&table[tok / BS]) : 0;
     }
   };
+  auto load_qf = [&](uint32_t (&qf)[NT][KS][2], const Item& it) {
+    if constexpr (FP8) load_q_f16<D, NT>(qf, it, lane, a);
+    else load_q<D, NT>(qf, it, lane, a);
+  };
   if (have_cur) {
     load_ids_w(ids_cur, cur);
-    load_q<D, NT>(qf_cur, cur, lane, a);
+    load_qf(qf_cur, cur);
     if (have_nxt) {
       load_ids_w(ids_nxt, nxt);
-      load_q<D, NT>(qf_nxt, nxt, lane, a);
+      load_qf(qf_nxt, nxt);
     }
   }
   PA_WEVENT(worker, 1);
@@ -965,8 +1099,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             } else {
 #pragma unroll
               for (int h = 0; h < KH; ++h) {
-                tma_load_2d(kdst + b * C::BOX_BYTES + h * ROWS * 128, &tmk, h * 64, y, fb);
-                tma_load_2d(vdst + b * C::BOX_BYTES + h * ROWS * 128, &tmv, h * 64, y, fb);
+                constexpr int kCols = FP8 ? 128 : 64;  // elements per 128-byte piece
+                tma_load_2d(kdst + b * C::BOX_BYTES + h * ROWS * 128, &tmk, h * kCols, y, fb);
+                tma_load_2d(vdst + b * C::BOX_BYTES + h * ROWS * 128, &tmv, h * kCols, y, fb);
               }
             }
           }
@@ -1020,7 +1155,11 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         }
         __syncwarp();
       }
-      attend_unit<D, ROWS, NT>(kb, vb, lane, nv, mask, a.scale_log2, qf_cur, acc, mrun, lrun);
+      if constexpr (FP8)
+        attend_unit_fp8<D, ROWS, NT>(kb, vb, lane, nv, mask, a.scale_log2, qf_cur, acc, mrun,
+                                     lrun);
+      else
+        attend_unit<D, ROWS, NT>(kb, vb, lane, nv, mask, a.scale_log2, qf_cur, acc, mrun, lrun);
       // The stage is refilled by this warp's next fill(); generic writes to
       // it (the zeroed rows) must be ordered before that TMA.
       if (!all_ok) fence_proxy_async_smem();
@@ -1045,14 +1184,17 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           const int n = t * 8 + 2 * (lane & 3) + (i & 1);
           if (n >= G) continue;
           const float l = lrun[t][i & 1];
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+          // fp8: the V scale rides on the output (and on the partials)
+          const float inv = (l > 0.f ? 1.f / l : 0.f) * (FP8 ? a.v_scale : 1.f);
+          const float pscale = FP8 ? a.v_scale : 1.f;
 #pragma unroll
           for (int dt = 0; dt < KS; ++dt) {
-            const int d = dt * 16 + (lane >> 2) + 8 * (i >> 1);
+            const int r = (lane >> 2) + 8 * (i >> 1);
+            const int d = FP8 ? fp8_out_d(dt, r) : dt * 16 + r;
             if (cur.part < 0)
               a.out[(row0 + n) * D + d] = __float2bfloat16_rn(acc[t][dt][i] * inv);
             else
-              a.ws_o[(prow + n) * D + d] = acc[t][dt][i];
+              a.ws_o[(prow + n) * D + d] = acc[t][dt][i] * pscale;
           }
         }
         if (cur.part >= 0 && lane < 4) {
@@ -1090,7 +1232,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt, kChunk);
     if (have_nxt) {
       load_ids_w(ids_nxt, nxt);
-      load_q<D, NT>(qf_nxt, nxt, lane, a);
+      load_qf(qf_nxt, nxt);
     }
   }
 
@@ -1225,20 +1367,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool as bf16 rows of D columns (num_blocks * n_kv * bs rows); a box
-// is `box_rows` rows of 64 columns (128 bytes, the swizzle span). For
-// D = 128 a 3-D view (64 columns, rows, 2 halves 128 bytes apart) lets one
-// copy fetch both halves of the rows; *map3d says which view was built.
-static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
-                                 int box_rows, bool try3d, int* map3d);
+// The pool as rows of D elements of eb bytes (num_blocks * n_kv * bs rows);
+// a box is `box_rows` rows of 128 bytes (the swizzle span): 64 bf16 columns
+// or 128 fp8 codes. For bf16 with D = 128 a 3-D view (64 columns, rows, 2
+// halves 128 bytes apart) lets one copy fetch both halves of the rows;
+// *map3d says which view was built.
+static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int eb,
+                                 int64_t rows, int box_rows, bool try3d, int* map3d);
 
 // Encoding a tensor map costs host time on every call; a decode loop reuses
 // the same pools, so keep the last few per thread.
-static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
+static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int eb, int64_t rows,
                                int box_rows, bool try3d, int* map3d) {
   struct Entry {
     const void* pool;
-    int D, box_rows, try3d, map3d;
+    int D, eb, box_rows, try3d, map3d;
     int64_t rows;
     CUtensorMap map;
   };
@@ -1246,18 +1389,19 @@ static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_
   static thread_local int used = 0, next = 0;
   for (int i = 0; i < used; ++i) {
     const Entry& e = cache[i];
-    if (e.pool == pool && e.D == D && e.rows == rows && e.box_rows == box_rows &&
-        e.try3d == (int)try3d) {
+    if (e.pool == pool && e.D == D && e.eb == eb && e.rows == rows &&
+        e.box_rows == box_rows && e.try3d == (int)try3d) {
       *map = e.map;
       *map3d = e.map3d;
       return PA_OK;
     }
   }
-  pa_status st = encode_pool_map(map, pool, D, rows, box_rows, try3d, map3d);
+  pa_status st = encode_pool_map(map, pool, D, eb, rows, box_rows, try3d, map3d);
   if (st != PA_OK) return st;
   Entry& e = cache[next];
   e.pool = pool;
   e.D = D;
+  e.eb = eb;
   e.rows = rows;
   e.box_rows = box_rows;
   e.try3d = (int)try3d;
@@ -1268,10 +1412,23 @@ static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int64_
   return PA_OK;
 }
 
-static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int64_t rows,
-                                 int box_rows, bool try3d, int* map3d) {
+static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int eb,
+                                 int64_t rows, int box_rows, bool try3d, int* map3d) {
   auto fn = encode_fn();
   if (!fn) return cuda_fail_msg("pa_decode", "cuTensorMapEncodeTiled unavailable");
+  if (eb == 1) {  // fp8 codes: one 128-byte row per token and head
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail_msg("pa_decode", "cuTensorMapEncodeTiled failed");
+    *map3d = 0;
+    return PA_OK;
+  }
   if (try3d && D == 128) {
     cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
@@ -1298,20 +1455,22 @@ static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int6
   return PA_OK;
 }
 
-template <int D, int BS, int NT>
+// FP8: E4M3 pools, balanced split only (a.balanced must be 1).
+template <int D, int BS, int NT, bool FP8 = false>
 static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
                         int64_t items_upper, cudaStream_t stream) {
   using C = Cfg<D, BS, NT>;
   auto kern = decode_kernel<D, BS, NT>;
   const int64_t rows = (int64_t)a.num_blocks * a.n_kv * BS;
+  constexpr int EB = FP8 ? 1 : 2;
   CUtensorMap tmk, tmv;
   int k3 = 0, v3 = 0;
-  pa_status st = make_pool_map(&tmk, k_pool, D, rows, C::ROWS, true, &k3);
+  pa_status st = make_pool_map(&tmk, k_pool, D, EB, rows, C::ROWS, !FP8, &k3);
   if (st != PA_OK) return st;
-  st = make_pool_map(&tmv, v_pool, D, rows, C::ROWS, k3 == 1, &v3);
+  st = make_pool_map(&tmv, v_pool, D, EB, rows, C::ROWS, k3 == 1, &v3);
   if (st != PA_OK) return st;
   if (k3 != v3) {  // both views must agree
-    st = make_pool_map(&tmk, k_pool, D, rows, C::ROWS, false, &k3);
+    st = make_pool_map(&tmk, k_pool, D, EB, rows, C::ROWS, false, &k3);
     if (st != PA_OK) return st;
   }
   a.map3d = k3 && v3;
@@ -1338,8 +1497,8 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   };
   static int cfg_item = 0, cfg_split = 0;
   static int occ_item[2] = {-1, 0}, occ_split[2] = {-1, 0};
-  auto skern = split_kernel<D, BS, NT>;
-  const size_t smem = a.balanced ? SplitCfg<D, BS, NT>::smem_bytes(a.num_seqs)
+  auto skern = split_kernel<D, BS, NT, FP8>;
+  const size_t smem = a.balanced ? SplitCfg<D, BS, NT, FP8>::smem_bytes(a.num_seqs)
                                  : C::smem_bytes(a.num_seqs, a.group);
   int occ = 0;
   st = a.balanced ? prepare(skern, smem, &cfg_split, occ_split, &occ)
@@ -1397,20 +1556,20 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   return PA_OK;
 }
 
-template <int D, int BS>
+template <int D, int BS, bool FP8>
 static pa_status dispatch_nt(const DecodeArgs& a, const void* kp, const void* vp, int64_t ub,
                              cudaStream_t st) {
-  if (a.group <= 8) return launch<D, BS, 1>(a, kp, vp, ub, st);
-  return launch<D, BS, 2>(a, kp, vp, ub, st);
+  if (a.group <= 8) return launch<D, BS, 1, FP8>(a, kp, vp, ub, st);
+  return launch<D, BS, 2, FP8>(a, kp, vp, ub, st);
 }
 
-template <int D>
+template <int D, bool FP8 = false>
 static pa_status dispatch_bs(int bs, const DecodeArgs& a, const void* kp, const void* vp,
                              int64_t ub, cudaStream_t st) {
   switch (bs) {
-    case 8: return dispatch_nt<D, 8>(a, kp, vp, ub, st);
-    case 16: return dispatch_nt<D, 16>(a, kp, vp, ub, st);
-    default: return dispatch_nt<D, 32>(a, kp, vp, ub, st);
+    case 8: return dispatch_nt<D, 8, FP8>(a, kp, vp, ub, st);
+    case 16: return dispatch_nt<D, 16, FP8>(a, kp, vp, ub, st);
+    default: return dispatch_nt<D, 32, FP8>(a, kp, vp, ub, st);
   }
 }
 
@@ -1488,13 +1647,20 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_k
   return w.total;
 }
 
-extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+namespace pa {
+
+// Checks and launch shared by pa_decode and pa_decode_fp8 (fp8: E4M3 pools,
+// head_dim 128, balanced split; the K scale joins the softmax scale).
+static pa_status decode_common(void* out, const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const int32_t* seq_lens,
                                int num_seqs, int max_blocks_per_seq, int num_blocks,
                                int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                                float scale, int partition_tokens, int max_seq_len,
                                void* workspace, size_t workspace_bytes, int32_t* err_word,
-                               pa_stream_t stream) {
+                               pa_stream_t stream, bool fp8, float k_scale, float v_scale) {
+  if (fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (fp8 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+    return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks_per_seq < 1 || num_blocks < 1 ||
       n_q_heads < 1 || n_kv_heads < 1 || max_seq_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -1538,12 +1704,43 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   a.part_tokens = P;
   a.max_parts = w.max_parts;
   a.len_cap = max_seq_len;
-  a.scale_log2 = scale * kLog2e;
+  a.scale_log2 = scale * (fp8 ? k_scale : 1.f) * kLog2e;
+  a.v_scale = fp8 ? v_scale : 1.f;
   a.map3d = 0;
   const int64_t items_upper = (int64_t)num_seqs * n_kv_heads * (w.max_parts > 0 ? w.max_parts : 1);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (fp8) return dispatch_bs<128, true>(block_size, a, k_pool, v_pool, items_upper, st);
   if (head_dim == 64) return dispatch_bs<64>(block_size, a, k_pool, v_pool, items_upper, st);
   return dispatch_bs<128>(block_size, a, k_pool, v_pool, items_upper, st);
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               int num_seqs, int max_blocks_per_seq, int num_blocks,
+                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                               float scale, int partition_tokens, int max_seq_len,
+                               void* workspace, size_t workspace_bytes, int32_t* err_word,
+                               pa_stream_t stream) {
+  return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                       max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim,
+                       block_size, scale, partition_tokens, max_seq_len, workspace,
+                       workspace_bytes, err_word, stream, false, 1.f, 1.f);
+}
+
+extern "C" pa_status pa_decode_fp8(void* out, const void* q, const void* k_pool,
+                                   const void* v_pool, const int32_t* block_tables,
+                                   const int32_t* seq_lens, int num_seqs,
+                                   int max_blocks_per_seq, int num_blocks, int n_q_heads,
+                                   int n_kv_heads, int head_dim, int block_size, float scale,
+                                   float k_scale, float v_scale, int max_seq_len,
+                                   void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                   pa_stream_t stream) {
+  return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                       max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim,
+                       block_size, scale, 0, max_seq_len, workspace, workspace_bytes, err_word,
+                       stream, true, k_scale, v_scale);
 }
 
 // ------------------------------------------------------------------ no-alloc

@@ -409,3 +409,64 @@ def make_values(wl: Workload, device="cpu", seed=None, poison_tails: bool = Fals
                     view = out[name].view(torch.int16)
                     view[blk, :, start:, :] = bits - (1 << 16 if bits >= 1 << 15 else 0)
     return out
+
+
+# fp8 (E4M3) cache contents. A full fp8 cache stands for K/V ~ N(0, 1) that
+# earlier steps stored with a per-tensor scale chosen so that about 4.5
+# standard deviations reach the largest code (448): scale = 4.5 / 448, a
+# value that is not a power of two, so the cache write's division rounds.
+FP8_SCALE = 4.5 / 448.0
+E4M3_NAN = 0x7F
+
+
+def make_values_fp8(wl: Workload, device="cpu", seed=None, poison_tails: bool = False,
+                    k_scale: float = FP8_SCALE, v_scale: float = FP8_SCALE):
+    """Like make_values, but k_pool/v_pool are uint8 E4M3 codes.
+
+    The pool codes are N(0, 1) / scale drawn in fp32 (on ``device``, seeded)
+    and cast by torch to float8_e4m3fn (torch's own conversion: how one draws fp8 data,
+    not the library's cache write). q and the new K/V stay bf16 N(0, 1).
+    With ``poison_tails`` the same slots as in make_values hold the NaN
+    code 0x7F in both pools."""
+    import torch
+
+    seed = wl.seed if seed is None else seed
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + 29)
+    S, Hq, Hkv, d, bs, NB = (wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                             wl.block_size, wl.num_blocks)
+    bf = torch.bfloat16
+
+    def codes(scale):
+        c = torch.empty((NB, Hkv, bs, d), dtype=torch.uint8, device=device)
+        step = max(1, (1 << 26) // max(1, Hkv * bs * d))  # bounded fp32 temporaries
+        for b0 in range(0, NB, step):
+            b1 = min(NB, b0 + step)
+            x = torch.randn((b1 - b0, Hkv, bs, d), generator=g, device=device,
+                            dtype=torch.float32) / scale
+            c[b0:b1] = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        return c
+
+    out = {
+        "q": torch.randn((S, Hq, d), generator=g, device=device, dtype=bf),
+        "k_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf),
+        "v_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf),
+        "k_pool": codes(k_scale),
+        "v_pool": codes(v_scale),
+    }
+    if poison_tails:
+        pair_src = {int(dst): int(src) for src, dst in wl.cow_pairs}
+        for s in range(S):
+            L = int(wl.seq_lens[s])
+            if L == 0:
+                continue
+            blk = int(wl.block_tables[s, (L - 1) // bs])
+            off = (L - 1) % bs
+            spans = [(blk, off + 1)]
+            if blk in pair_src:
+                spans.append((pair_src[blk], off))
+            for b, start in spans:
+                if start < bs:
+                    out["k_pool"][b, :, start:, :] = E4M3_NAN
+                    out["v_pool"][b, :, start:, :] = E4M3_NAN
+    return out

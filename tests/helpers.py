@@ -65,11 +65,12 @@ def oracle_step(wl: W.Workload, vals_cpu: dict):
     return out, kp, vp
 
 
-def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs):
+def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs, fp8_scales=None):
     """Oracle rows for the sequences `seqs` of a workload too large to copy
     whole: gather (before the GPU step touches the pool) only the blocks
     those sequences read, plus their copy-on-write sources, into a compact
-    host pool, remap ids, and run the oracle's step there.
+    host pool, remap ids, and run the oracle's step there. fp8_scales =
+    (k_scale, v_scale) for uint8 E4M3 pools.
     Returns out fp64 [len(seqs), Hq, d]."""
     bs = wl.block_size
     seqs = list(seqs)
@@ -84,8 +85,9 @@ def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs):
     ids = list(dict.fromkeys(need))
     remap = {b: i for i, b in enumerate(ids)}
     idx = torch.tensor(ids, dtype=torch.long, device=vals_dev["k_pool"].device)
-    kp = bits(vals_dev["k_pool"].index_select(0, idx)).copy()
-    vp = bits(vals_dev["v_pool"].index_select(0, idx)).copy()
+    pool_np = bits if fp8_scales is None else (lambda t: t.cpu().numpy())
+    kp = pool_np(vals_dev["k_pool"].index_select(0, idx)).copy()
+    vp = pool_np(vals_dev["v_pool"].index_select(0, idx)).copy()
     maxb = wl.block_tables.shape[1]
     bt = np.full((len(seqs), maxb), -1, np.int32)
     slots, pairs = [], []
@@ -101,9 +103,17 @@ def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs):
     q = bits(vals_dev["q"].index_select(0, sel))
     kn = bits(vals_dev["k_new"].index_select(0, sel))
     vn = bits(vals_dev["v_new"].index_select(0, sel))
-    paref.copy_blocks(kp, vp, np.array(pairs, np.int32).reshape(-1, 2))
-    paref.reshape_and_cache(kn, vn, kp, vp, np.array(slots, np.int32))
-    return paref.attention_paged(q, kp, vp, bt, wl.seq_lens[seqs].astype(np.int32), wl.scale)
+    pairs = np.array(pairs, np.int32).reshape(-1, 2)
+    slots = np.array(slots, np.int32)
+    lens = wl.seq_lens[seqs].astype(np.int32)
+    if fp8_scales is None:
+        paref.copy_blocks(kp, vp, pairs)
+        paref.reshape_and_cache(kn, vn, kp, vp, slots)
+        return paref.attention_paged(q, kp, vp, bt, lens, wl.scale)
+    ks, vs = fp8_scales
+    paref.copy_blocks(kp.view(np.uint16), vp.view(np.uint16), pairs)  # a byte copy
+    paref.reshape_and_cache_fp8(kn, vn, kp, vp, slots, ks, vs)
+    return paref.attention_paged_fp8(q, kp, vp, bt, lens, wl.scale, ks, vs)
 
 
 def compare(gpu_out: torch.Tensor, ref: np.ndarray, what=""):
@@ -120,3 +130,42 @@ def compare(gpu_out: torch.Tensor, ref: np.ndarray, what=""):
     assert max_abs <= ATOL, f"{what}: max abs err {max_abs:.3e} > {ATOL}"
     assert max_rel <= ROW_RTOL, f"{what}: max row rel err {max_rel:.3e} > {ROW_RTOL}"
     return max_abs, max_rel
+
+
+# ------------------------------------------------------------------ fp8 cache
+
+def gpu_step_fp8(wl: W.Workload, vals: dict, k_scale, v_scale, workspace=None, err=None,
+                 run_writes=True):
+    """copy_blocks_fp8 -> reshape_and_cache_fp8 -> decode_fp8 (pools are
+    uint8 E4M3 codes, modified in place). Returns (out, err_word value)."""
+    dev = vals["q"].device
+    t = to_dev(wl, dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                                       wl.block_size, wl.max_seq_len, 0, device=dev)
+    out = torch.full_like(vals["q"], float("nan"))
+    if run_writes:
+        B.pa_copy_blocks_fp8(vals["k_pool"], vals["v_pool"], t["pairs"], err_word=err)
+        B.pa_reshape_and_cache_fp8(vals["k_new"], vals["v_new"], vals["k_pool"],
+                                   vals["v_pool"], t["slot_mapping"], k_scale, v_scale,
+                                   err_word=err)
+    B.pa_decode_fp8(out, vals["q"], vals["k_pool"], vals["v_pool"], t["block_tables"],
+                    t["seq_lens"], wl.scale, k_scale, v_scale, max_seq_len=wl.max_seq_len,
+                    workspace=workspace, err_word=err)
+    torch.cuda.synchronize()
+    return out, int(err.item())
+
+
+def oracle_step_fp8(wl: W.Workload, vals_cpu: dict, k_scale, v_scale):
+    """The oracle's step over uint8 E4M3 pools. Returns (out, k codes, v codes)."""
+    kp = vals_cpu["k_pool"].numpy().copy()
+    vp = vals_cpu["v_pool"].numpy().copy()
+    # a block copy moves bytes: the oracle's copy on a 16-bit view of the codes
+    paref.copy_blocks(kp.view(np.uint16), vp.view(np.uint16), wl.cow_pairs)
+    paref.reshape_and_cache_fp8(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
+                                wl.slot_mapping, k_scale, v_scale)
+    out = paref.attention_paged_fp8(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
+                                    wl.scale, k_scale, v_scale)
+    return out, kp, vp
