@@ -12,7 +12,10 @@ Metric: KV bytes the step must read (sum of lengths x kv heads x head_dim x
 2 bytes x K,V) per second of device time, plus tokens attended per second.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 1..5] [--block-size 8|16|32]
+                    [--config 1..5] [--block-size 8|16|32] [--kv bf16|fp8]
+
+With --kv fp8 the pools hold E4M3 codes (one byte per element, per-tensor
+scales): the same step through the fp8 entry points, KV bytes halved.
 """
 from __future__ import annotations
 
@@ -48,6 +51,8 @@ def parse():
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                   help="KV cache element type (fp8: E4M3 codes with per-tensor scales)")
     p.add_argument("--eager", action="store_true",
                    help="launch every call from Python instead of replaying CUDA graphs")
     return p.parse_args()
@@ -165,21 +170,30 @@ def _bits(t):
     return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def cpu_oracle_step(wl, vals_cpu, seqs):
+def cpu_oracle_step(wl, vals_cpu, seqs, fp8_scale=None):
     """The oracle's copy -> write -> attention for the sequences `seqs`
-    (a bounded sample of the workload). Returns KV bytes of the sample."""
+    (a bounded sample of the workload); fp8_scale: E4M3 pools with that
+    scale for K and V. Returns KV bytes of the sample."""
     import numpy as np
     from oracle import paref
     bits = _bits
+    rows = np.array([(s, h) for s in seqs for h in range(wl.n_q_heads)], np.int32)
+    ntok = int(wl.seq_lens[list(seqs)].astype(np.int64).sum())
+    if fp8_scale is not None:
+        kp, vp = vals_cpu["k_pool"].numpy().copy(), vals_cpu["v_pool"].numpy().copy()
+        paref.copy_blocks(kp.view(np.uint16), vp.view(np.uint16), wl.cow_pairs)
+        paref.reshape_and_cache_fp8(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
+                                    wl.slot_mapping, fp8_scale, fp8_scale)
+        paref.attention_paged_fp8(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
+                                  wl.scale, fp8_scale, fp8_scale, rows=rows)
+        return ntok * wl.n_kv_heads * wl.head_dim * 1 * 2
     kp, vp = bits(vals_cpu["k_pool"]).copy(), bits(vals_cpu["v_pool"]).copy()
     paref.copy_blocks(kp, vp, wl.cow_pairs)
     paref.reshape_and_cache(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
                             wl.slot_mapping)
-    rows = np.array([(s, h) for s in seqs for h in range(wl.n_q_heads)], np.int32)
     paref.attention_paged(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
                           wl.scale, rows=rows)
-    return int(wl.seq_lens[list(seqs)].astype(np.int64).sum()) * wl.n_kv_heads * \
-        wl.head_dim * 2 * 2
+    return ntok * wl.n_kv_heads * wl.head_dim * 2 * 2
 
 
 def cpu_sample_seqs(wl, budget_tokens):
@@ -204,20 +218,22 @@ def run_reference(args):
     wl = build_workload(args.config, args.block_size)
     budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
     seqs, tok = cpu_sample_seqs(wl, budget)
-    vals = W_make_values_subset(wl, seqs)
+    fp8 = fp8_scale_of(args)
+    vals = W_make_values_subset(wl, seqs, fp8=fp8 is not None)
     for _ in range(max(0, args.warmup)):
-        cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"])
+        cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"], fp8)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"])
+        nbytes += cpu_oracle_step(vals["wl"], vals["vals"], vals["seqs"], fp8)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / max(1, args.steps) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample_seqs": len(seqs), "sample_tokens": tok},
+            "config": {"workload": wl.name, "kv_dtype": args.kv, "sample_seqs": len(seqs),
+                       "sample_tokens": tok},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{len(seqs)} of {wl.num_seqs} sequences "
                                        f"({tok} tokens) per step, all query heads"},
@@ -226,7 +242,14 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def W_make_values_subset(wl, seqs):
+def fp8_scale_of(args):
+    if args.kv != "fp8":
+        return None
+    from paged_kv_cache_105_gb300 import workloads as W
+    return W.FP8_SCALE
+
+
+def W_make_values_subset(wl, seqs, fp8=False):
     """A self-contained sub-workload holding only `seqs` (tables remapped
     onto a compact pool), with values drawn for exactly those blocks, so the
     CPU baseline never allocates the full pool on the host."""
@@ -260,7 +283,7 @@ def W_make_values_subset(wl, seqs):
                      block_tables=bt, slot_mapping=np.array(slots, np.int32),
                      cow_pairs=np.array(pairs, np.int32).reshape(-1, 2),
                      free_order=np.arange(max(1, len(ids)), dtype=np.int32), seed=wl.seed)
-    vals = W.make_values(sub, device="cpu")
+    vals = W.make_values_fp8(sub, device="cpu") if fp8 else W.make_values(sub, device="cpu")
     return {"wl": sub, "vals": vals, "seqs": list(range(len(seqs)))}
 
 
@@ -283,13 +306,17 @@ def main():
     from paged_kv_cache_105_gb300 import workloads as W
 
     wl = build_workload(args.config, args.block_size)
+    fp8 = fp8_scale_of(args)
     P = wl.partition_tokens if args.partition_tokens is None else args.partition_tokens
+    if fp8 is not None:
+        P = 0  # the fp8 decode always runs the balanced split
     P_res = B.pa_decode_partition_tokens(wl.num_seqs, wl.n_kv_heads, wl.block_size,
                                          wl.max_seq_len, P)
-    base = W.make_values(wl, device=dev)
-    pool_bytes = 2 * base["k_pool"].numel() * 2
+    eb = 1 if fp8 is not None else 2  # bytes per cached element
+    base = W.make_values_fp8(wl, device=dev) if fp8 is not None else W.make_values(wl, device=dev)
+    pool_bytes = 2 * base["k_pool"].numel() * eb
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    replicas = max(1, math.ceil(3 * l2 / max(1, wl.kv_bytes())))
+    replicas = max(1, math.ceil(3 * l2 / max(1, wl.kv_bytes(eb))))
     replicas = min(replicas, max(1, int(40e9 // max(1, pool_bytes))))
     reps = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(replicas - 1)]
     t = {"bt": torch.from_numpy(wl.block_tables).to(dev),
@@ -306,17 +333,32 @@ def main():
                          + (1 if wl.num_seqs else 0) + (1 if (P == 0 or max_parts > 1) else 0))
     stream = torch.cuda.current_stream(dev)
 
-    def calls_write(r):
+    def api_write(r, pairs, k_new, v_new, sm):
+        if fp8 is not None:
+            if n_pairs:
+                B.pa_copy_blocks_fp8(r["k_pool"], r["v_pool"], pairs, err_word=err)
+            B.pa_reshape_and_cache_fp8(k_new, v_new, r["k_pool"], r["v_pool"], sm, fp8, fp8,
+                                       err_word=err)
+            return
         if n_pairs:
-            B.pa_copy_blocks(r["k_pool"], r["v_pool"], t["pairs"], err_word=err)
-        B.pa_reshape_and_cache(r["k_new"], r["v_new"], r["k_pool"], r["v_pool"], t["sm"],
-                               err_word=err)
+            B.pa_copy_blocks(r["k_pool"], r["v_pool"], pairs, err_word=err)
+        B.pa_reshape_and_cache(k_new, v_new, r["k_pool"], r["v_pool"], sm, err_word=err)
+
+    def api_decode(out, q, r, bt, sl, ws):
+        if fp8 is not None:
+            B.pa_decode_fp8(out, q, r["k_pool"], r["v_pool"], bt, sl, wl.scale, fp8, fp8,
+                            max_seq_len=wl.max_seq_len, workspace=ws, err_word=err)
+        else:
+            B.pa_decode(out, q, r["k_pool"], r["v_pool"], bt, sl, wl.scale,
+                        max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=P,
+                        err_word=err)
+
+    def calls_write(r):
+        api_write(r, t["pairs"], r["k_new"], r["v_new"], t["sm"])
 
     def calls_decode(j):
         r = reps[j]
-        B.pa_decode(outs[j], r["q"], r["k_pool"], r["v_pool"], t["bt"], t["sl"],
-                    wl.scale, max_seq_len=wl.max_seq_len, workspace=wss[j],
-                    partition_tokens=P, err_word=err)
+        api_decode(outs[j], r["q"], r, t["bt"], t["sl"], wss[j])
 
     # Eager warm-up (also the library's one-time set-up), then, unless
     # --eager, one CUDA graph per replica for the writes and one for the
@@ -413,7 +455,7 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
 
-    kv_bytes = wl.kv_bytes()
+    kv_bytes = wl.kv_bytes(eb)
     alg_bytes = kv_bytes + wl.io_bytes()
     ms_per_step = total_ms / args.steps
     value = world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9
@@ -443,13 +485,9 @@ def main():
             dev_in[k].copy_(host[k], non_blocking=True)
         for k in host_idx:
             dev_idx[k].copy_(host_idx[k], non_blocking=True)
-        if n_pairs:
-            B.pa_copy_blocks(r["k_pool"], r["v_pool"], dev_idx["pairs"], err_word=err)
-        B.pa_reshape_and_cache(dev_in["k_new"], dev_in["v_new"], r["k_pool"], r["v_pool"],
-                               dev_idx["sm"], err_word=err)
-        B.pa_decode(outs[i % replicas], dev_in["q"], r["k_pool"], r["v_pool"], dev_idx["bt"],
-                    dev_idx["sl"], wl.scale, max_seq_len=wl.max_seq_len,
-                    workspace=wss[i % replicas], partition_tokens=P, err_word=err)
+        api_write(r, dev_idx["pairs"], dev_in["k_new"], dev_in["v_new"], dev_idx["sm"])
+        api_decode(outs[i % replicas], dev_in["q"], r, dev_idx["bt"], dev_idx["sl"],
+                   wss[i % replicas])
         host_out.copy_(outs[i % replicas], non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()  # the caller needs the result
 
@@ -475,10 +513,13 @@ def main():
 
     peak, peak_kind = measured_peak()
     achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name)
+    traffic = recorded_traffic(wl.name + ("-fp8" if fp8 is not None else ""))
+    kname = ("split_kernel<fp8> (pa_decode_fp8) + merge_kernel" if fp8 is not None else
+             "split_kernel (pa_decode, balanced split) + merge_kernel" if P == 0 else
+             "decode_kernel (pa_decode, fixed partitions) + merge_kernel")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "decode_kernel (pa_decode)",
+                "kernel": kname,
                 "peak_source": f"{peak_kind} hbm_gbs",
                 "alg_bytes_per_launch": alg_bytes,
                 "timing": ("CUDA events around each decode launch inside the timed steps"
@@ -491,13 +532,13 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
         seqs, tok = cpu_sample_seqs(wl, budget)
-        sub = W_make_values_subset(wl, seqs)
-        cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"])  # load + warm
+        sub = W_make_values_subset(wl, seqs, fp8=fp8 is not None)
+        cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"], fp8)  # load + warm
         c0 = time.perf_counter()
         reps_cpu = 0
         nbytes = 0
         while True:
-            nbytes += cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"])
+            nbytes += cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"], fp8)
             reps_cpu += 1
             if time.perf_counter() - c0 > 10.0 or reps_cpu >= 1000:
                 break
@@ -510,16 +551,20 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if fp8 is None else "e4m3 K/V, bf16 q/out",
         "data": "synthetic",
-        "config": {"workload": wl.name, "num_seqs": wl.num_seqs,
+        "config": {"workload": wl.name, "kv_dtype": args.kv, "num_seqs": wl.num_seqs,
                    "tokens_attended": wl.tokens_attended, "n_q_heads": wl.n_q_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "partition_tokens": P_res,
                    "cow_pairs": n_pairs, "kv_bytes_per_step": kv_bytes,
                    "l2": f"inputs rotated over {replicas} replicas "
                          f"({replicas * kv_bytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2)",
-                   "arithmetic": "bf16 operands, fp32 accumulation and softmax",
+                   "arithmetic": ("bf16 operands, fp32 accumulation and softmax"
+                                  if fp8 is None else
+                                  "E4M3 codes and q as f16 mma operands, fp32 accumulation "
+                                  "and softmax; per-tensor scales"),
                    "launch": "eager calls from Python" if args.eager else
                              "one CUDA graph replay per step (copy, write, decode, merge)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

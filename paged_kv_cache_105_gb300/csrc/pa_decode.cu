@@ -22,7 +22,8 @@
 //  * The GQA group (the G query heads sharing the kv head) is the N side of
 //    bf16 mma.sync m16n8k16 with the tokens on M: S^T = K Q^T, then
 //    O^T += V^T P^T; movmatrix turns the score fragment into the P^T operand
-//    in registers. Online softmax in fp32, base 2.
+//    in registers. Online softmax in fp32, base 2; the running maximum is
+//    moved (and the state rescaled) only when a score exceeds it by 2^8.
 //  * Warps 1-3 hand their state to warp 0 through shared memory; a
 //    one-partition sequence writes its bf16 output directly, otherwise the
 //    partition's (O, m, l) goes to the workspace and a second, small kernel
@@ -330,6 +331,71 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Item
   }
 }
 
+// Online softmax of one unit's scores, base 2, with a lazily moved
+// reference: m (per query head) only moves when some score exceeds it by
+// more than kLazyLog2, and then the accumulators and sums are rescaled to the
+// new maximum; otherwise the weights 2^(x - m) are used as they are. They
+// stay below 2^kLazyLog2, which the fp32 sums and the 16-bit P operand hold
+// exactly as well as weights below 1. (m, l) keep their meaning: l is the sum
+// of 2^(x - m) and O the matching weighted sum, whatever m is. sc holds the
+// raw scores of tokens tA = g (sc[..][0..1]) and tB = g + 8 (sc[..][2..3]);
+// masked tokens weigh zero. P^T fragments come back in pb (f16 or bf16).
+constexpr float kLazyLog2 = 8.f;
+
+template <int NT, int KS, bool F16P>
+__device__ __forceinline__ void softmax_unit(const float (&sc)[NT][4], bool okA, bool okB,
+                                             float scale_log2, float (&acc)[NT][KS][4],
+                                             float (&mrun)[NT][2], float (&lrun)[NT][2],
+                                             uint32_t (&pb)[NT][2]) {
+  float x[NT][4];
+  bool need = false;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      x[t][jj] = okA ? sc[t][jj] * scale_log2 : -INFINITY;
+      x[t][jj + 2] = okB ? sc[t][jj + 2] * scale_log2 : -INFINITY;
+      need |= fmaxf(x[t][jj], x[t][jj + 2]) > mrun[t][jj] + kLazyLog2;
+    }
+  }
+  if (__any_sync(0xffffffffu, need)) {  // warp-uniform: move the reference
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const float mx = warp_max_xor4(fmaxf(x[t][jj], x[t][jj + 2]));
+        const float m_new = fmaxf(mrun[t][jj], mx);
+        const float alpha = fast_exp2(mrun[t][jj] - (m_new == -INFINITY ? 0.f : m_new));
+        lrun[t][jj] *= alpha;
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+          acc[t][dt][jj] *= alpha;
+          acc[t][dt][jj + 2] *= alpha;
+        }
+        mrun[t][jj] = m_new;
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float pv[4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const float base = mrun[t][jj] == -INFINITY ? 0.f : mrun[t][jj];
+      pv[jj] = fast_exp2(x[t][jj] - base);
+      pv[jj + 2] = fast_exp2(x[t][jj + 2] - base);
+      lrun[t][jj] += pv[jj] + pv[jj + 2];
+    }
+    if constexpr (F16P) {
+      pb[t][0] = movmatrix_trans(pack_f16x2(pv[0], pv[1]));
+      pb[t][1] = movmatrix_trans(pack_f16x2(pv[2], pv[3]));
+    } else {
+      pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
+      pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
+    }
+  }
+}
+
 // One 16-token unit of attention for the warp, online softmax in base 2.
 // K and V rows sit in shared memory (128-byte swizzled tiles, one box of
 // ROWS rows per block); tokens >= nv or in a box whose bit is clear in
@@ -367,30 +433,7 @@ __device__ __forceinline__ void attend_unit(uint32_t kb, uint32_t vb, int lane, 
     const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
     const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
     uint32_t pb[NT][2];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float pv[4];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const float xa = okA ? sc[t][jj] * scale_log2 : -INFINITY;
-        const float xb = okB ? sc[t][jj + 2] * scale_log2 : -INFINITY;
-        const float mx = warp_max_xor4(fmaxf(xa, xb));
-        const float m_new = fmaxf(mrun[t][jj], mx);
-        const float base = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = fast_exp2(mrun[t][jj] - base);
-        pv[jj] = fast_exp2(xa - base);
-        pv[jj + 2] = fast_exp2(xb - base);
-        lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
-        mrun[t][jj] = m_new;
-#pragma unroll
-        for (int dt = 0; dt < KS; ++dt) {
-          acc[t][dt][jj] *= alpha;
-          acc[t][dt][jj + 2] *= alpha;
-        }
-      }
-      pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
-      pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
-    }
+    softmax_unit<NT, KS, false>(sc, okA, okB, scale_log2, acc, mrun, lrun, pb);
     // ---- O^T += V^T P^T
     {
       const int mi = lane >> 3;
@@ -491,30 +534,7 @@ __device__ __forceinline__ void attend_unit_fp8(uint32_t kb, uint32_t vb, int la
   const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
   const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
   uint32_t pb[NT][2];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    float pv[4];
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const float xa = okA ? sc[t][jj] * scale_log2 : -INFINITY;
-      const float xb = okB ? sc[t][jj + 2] * scale_log2 : -INFINITY;
-      const float mx = warp_max_xor4(fmaxf(xa, xb));
-      const float m_new = fmaxf(mrun[t][jj], mx);
-      const float base = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = fast_exp2(mrun[t][jj] - base);
-      pv[jj] = fast_exp2(xa - base);
-      pv[jj + 2] = fast_exp2(xb - base);
-      lrun[t][jj] = lrun[t][jj] * alpha + pv[jj] + pv[jj + 2];
-      mrun[t][jj] = m_new;
-#pragma unroll
-      for (int dt = 0; dt < KS; ++dt) {
-        acc[t][dt][jj] *= alpha;
-        acc[t][dt][jj + 2] *= alpha;
-      }
-    }
-    pb[t][0] = movmatrix_trans(pack_f16x2(pv[0], pv[1]));
-    pb[t][1] = movmatrix_trans(pack_f16x2(pv[2], pv[3]));
-  }
+  softmax_unit<NT, KS, true>(sc, okA, okB, scale_log2, acc, mrun, lrun, pb);
   // ---- O^T += V^T P^T
 #pragma unroll
   for (int p = 0; p < KS / 2; ++p) {

@@ -205,3 +205,32 @@ def test_length_beyond_hint_is_clamped_and_flagged():
     clamped.seq_lens = np.array([80, 64], np.int32)
     ref, _, _ = oracle_step(clamped, vals_cpu)
     compare(out, ref, "clamped")
+
+
+def _rising(wl, kpool, knew, gain):
+    """Scale token i's K by (1 + gain * i) in place (pool rows and new tokens),
+    so that scores grow along each sequence and the running maximum keeps
+    moving by large steps."""
+    bs = wl.block_size
+    for s in range(wl.num_seqs):
+        L = int(wl.seq_lens[s])
+        for i in range(L - 1):
+            b = int(wl.block_tables[s, i // bs])
+            kpool[b, :, i % bs, :] *= 1.0 + gain * i
+        if L:
+            knew[s] *= 1.0 + gain * (L - 1)
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+def test_rising_scores_move_the_running_max(partition_tokens):
+    wl = W.custom([1000, 300, 17, 64], n_q_heads=16, n_kv_heads=4, seed=21, name="rising")
+    vals_cpu = W.make_values(wl)
+    kp = vals_cpu["k_pool"].float()
+    kn = vals_cpu["k_new"].float()
+    _rising(wl, kp, kn, 0.05)
+    vals_cpu["k_pool"] = kp.to(torch.bfloat16)
+    vals_cpu["k_new"] = kn.to(torch.bfloat16)
+    ref, _, _ = oracle_step(wl, vals_cpu)
+    out, err = gpu_step(wl, on_dev(vals_cpu), partition_tokens=partition_tokens)
+    assert err == 0
+    compare(out, ref, "rising")

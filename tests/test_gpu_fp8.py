@@ -144,3 +144,27 @@ def test_fp8_unsupported_and_invalid_arguments():
         B.pa_reshape_and_cache_fp8(vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"],
                                    t["slot_mapping"], 0.0, VS)
     assert e.value.status == B.PA_ERR_INVALID_ARG
+
+
+def test_fp8_rising_scores_move_the_running_max():
+    # codes drawn from N(0, 1) * (1 + 0.1 i) / scale: scores grow along the
+    # sequence, so the running maximum keeps moving by large steps
+    wl = W.custom([900, 250, 33], n_q_heads=16, n_kv_heads=4, seed=22, name="fp8-rising")
+    k_scale = 0.25
+    vals_cpu = W.make_values_fp8(wl, k_scale=k_scale)
+    g = torch.Generator().manual_seed(7)
+    kp = torch.randn(vals_cpu["k_pool"].shape, generator=g)
+    kn = vals_cpu["k_new"].float()
+    bs = wl.block_size
+    for s in range(wl.num_seqs):
+        L = int(wl.seq_lens[s])
+        for i in range(L - 1):
+            kp[int(wl.block_tables[s, i // bs]), :, i % bs, :] *= 1.0 + 0.1 * i
+        kn[s] *= 1.0 + 0.1 * (L - 1)
+    vals_cpu["k_pool"] = (kp / k_scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    vals_cpu["k_new"] = kn.to(torch.bfloat16)
+    ref, _, _ = oracle_step_fp8(wl, vals_cpu, k_scale, VS)
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
+    out, err = gpu_step_fp8(wl, vals, k_scale, VS)
+    assert err == 0
+    compare(out, ref, "fp8-rising")
