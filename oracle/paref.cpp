@@ -351,6 +351,24 @@ extern "C" int paref_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32
   return skipped;
 }
 
+extern "C" int paref_swap_blocks(uint8_t* dst_k, uint8_t* dst_v, const uint8_t* src_k,
+                                 const uint8_t* src_v, const int32_t* pairs, int n_pairs,
+                                 int64_t block_bytes, int src_num_blocks, int dst_num_blocks) {
+  int skipped = 0;
+  for (int p = 0; p < n_pairs; ++p) {
+    const int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+      ++skipped;
+      continue;
+    }
+    for (int64_t b = 0; b < block_bytes; ++b) {
+      dst_k[dst * block_bytes + b] = src_k[src * block_bytes + b];
+      dst_v[dst * block_bytes + b] = src_v[src * block_bytes + b];
+    }
+  }
+  return skipped;
+}
+
 // ---------------------------------------------------------------------------
 // FP8 E4M3 (OCP FP8 formats): sign, 4 exponent bits with bias 7, 3 mantissa
 // bits. Exponent field 0 is subnormal (value m * 2^-9); the all-ones

@@ -125,6 +125,21 @@ int paref_reshape_and_cache(const uint16_t* k, const uint16_t* v, uint16_t* k_po
 int paref_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* pairs, int n_pairs,
                       int n_kv_heads, int head_dim, int block_size, int num_blocks);
 
+/* ---------------- swap ("03 · PagedAttention", "Memory management, in
+   brief": when memory runs out a sequence can be preempted by swapping its
+   blocks out to CPU memory and back in later; "Serving: vLLM and
+   PagedAttention", preemption by swapping) ---------------------------- */
+
+/* For each (src, dst) pair: block dst of the destination pools becomes a
+   byte copy of block src of the source pools (K and V), where a block is
+   block_bytes bytes (n_kv_heads * block_size * head_dim * element size).
+   The two sides are different pools (device and host memory in the GPU
+   path). Returns the number of pairs skipped for an id outside the source
+   or destination pool. */
+int paref_swap_blocks(uint8_t* dst_k, uint8_t* dst_v, const uint8_t* src_k, const uint8_t* src_v,
+                      const int32_t* pairs, int n_pairs, int64_t block_bytes,
+                      int src_num_blocks, int dst_num_blocks);
+
 /* ---------------- FP8 KV cache ("PagedAttention" (mlapandio.dev), Cons and
    honest limits, and "Serving: vLLM and PagedAttention" section 3.1: an fp8
    KV cache halves the cache and the bytes read per step). The format is

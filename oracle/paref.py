@@ -59,6 +59,8 @@ def lib():
                                                       C.c_int, C.c_int, C.c_int, C.c_int]),
                 "paref_copy_blocks": (C.c_int, [u16p, u16p, i32p, C.c_int, C.c_int, C.c_int,
                                                 C.c_int, C.c_int]),
+                "paref_swap_blocks": (C.c_int, [u8p, u8p, u8p, u8p, i32p, C.c_int, C.c_int64,
+                                                C.c_int, C.c_int]),
                 "paref_e4m3_decode": (C.c_double, [C.c_uint8]),
                 "paref_e4m3_encode": (C.c_uint8, [C.c_double]),
                 "paref_reshape_and_cache_fp8": (C.c_int, [u16p, u16p, u8p, u8p, i32p, C.c_int,
@@ -275,6 +277,30 @@ def copy_blocks(k_pool, v_pool, pairs) -> int:
     pr, prp = _i32(np.asarray(pairs).reshape(-1, 2))
     NB, Hkv, bs, d = k_pool.shape
     return lib().paref_copy_blocks(kpp, vpp, prp, pr.shape[0], Hkv, d, bs, NB)
+
+
+# ----------------------------------------------------------------- swap
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs) -> int:
+    """Block pairs[p, 1] of the destination pools becomes a byte copy of block
+    pairs[p, 0] of the source pools. Pools are C-contiguous arrays whose
+    first axis is the block id (any element type: the copy is of bytes).
+    Returns the skipped count."""
+    arrs = []
+    for a in (dst_k, dst_v, src_k, src_v):
+        a = np.asarray(a)
+        if not a.flags["C_CONTIGUOUS"]:
+            raise TypeError("pools must be C-contiguous")
+        arrs.append(a)
+    dk, dv, sk, sv = arrs
+    if dk.shape[1:] != sk.shape[1:] or dk.dtype != sk.dtype or dv.shape != dk.shape or \
+            sv.shape != sk.shape:
+        raise ValueError("source and destination blocks must have one shape")
+    block_bytes = dk[0].nbytes if len(dk) else sk[0].nbytes
+    pr, prp = _i32(np.asarray(pairs).reshape(-1, 2))
+    u8 = lambda a: a.ctypes.data_as(u8p)
+    return lib().paref_swap_blocks(u8(dk), u8(dv), u8(sk), u8(sv), prp, pr.shape[0],
+                                   int(block_bytes), sk.shape[0], dk.shape[0])
 
 
 # ----------------------------------------------------------------- fp8 (E4M3)
