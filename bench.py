@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--op", choices=["decode", "swap"], default="decode",
+                   help="decode: the decode step (default); swap: block swap-out to pinned "
+                        "host memory and swap-in back")
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales)")
     p.add_argument("--eager", action="store_true",
@@ -287,10 +290,91 @@ def W_make_values_subset(wl, seqs, fp8=False):
     return {"wl": sub, "vals": vals, "seqs": list(range(len(seqs)))}
 
 
+def run_swap(args):
+    """Preemption by swapping: every block the workload's tables use goes to a
+    pinned host pool (swap-out) and comes back to the same ids (swap-in);
+    one step = both. Compared with the copy engine moving the same bytes as
+    one contiguous buffer each way (torch copy_, device <-> pinned host)."""
+    import numpy as np
+    import torch
+    world, rank, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_105_gb300 import binding as B
+    from paged_kv_cache_105_gb300 import workloads as W
+    wl = build_workload(args.config, args.block_size)
+    fp8 = fp8_scale_of(args)
+    vals = W.make_values_fp8(wl, device=dev) if fp8 is not None else W.make_values(wl, device=dev)
+    gk, gv = vals["k_pool"], vals["v_pool"]
+    ids = np.unique(wl.block_tables[wl.block_tables >= 0]).astype(np.int32)
+    n = len(ids)
+    hk = torch.empty((n,) + tuple(gk.shape[1:]), dtype=gk.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([ids, np.arange(n, dtype=np.int32)], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), ids], 1)).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    block_bytes = gk[0].numel() * gk.element_size()
+    moved = 2 * 2 * n * block_bytes  # K and V, out and in
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.pa_swap_blocks(hk, hv, gk, gv, out_pairs, err_word=err)
+        B.pa_swap_blocks(gk, gv, hk, hv, in_pairs, err_word=err)
+
+    dbuf = torch.empty(2 * n * block_bytes, dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(dbuf.shape, dtype=torch.uint8).pin_memory()
+
+    def ce_step():
+        hbuf.copy_(dbuf, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    res = {}
+    for name, fn in (("kernel", step), ("copy_engine", ce_step)):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+    if rank != 0:
+        return
+    gbs = moved / (res["kernel"] * 1e-3) / 1e9
+    ce = moved / (res["copy_engine"] * 1e-3) / 1e9
+    line = {"metric": "KV block swap, device <-> pinned host (out + in) GB/s", "value": gbs,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["kernel"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8 (byte copy)", "data": "synthetic",
+            "config": {"workload": wl.name, "kv_dtype": args.kv, "blocks": n,
+                       "block_bytes": block_bytes, "bytes_per_step": moved,
+                       "l2": f"{moved / 2e6:.0f} MB per direction vs "
+                             f"{torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB L2"},
+            "roofline": {"bound": "chip-to-chip link", "achieved": gbs, "peak": ce,
+                         "unit": "GB/s", "frac": gbs / ce, "traffic": None,
+                         "kernel": "swap_blocks_kernel (pa_swap_blocks) x2",
+                         "peak_source": "copy engine moving the same bytes as one contiguous "
+                                        "buffer each way, measured in this run"},
+            "gpu_launches": 2 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.op == "swap":
+        run_swap(args)
         return
 
     import numpy as np

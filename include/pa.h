@@ -282,6 +282,36 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* k_pool, const void
                         int32_t* err_word, pa_stream_t stream);
 
 /*
+ * pa_swap_blocks — copy whole blocks between two pools, one of which is
+ * normally in host memory: preemption by swapping. "03 · PagedAttention",
+ * "Memory management, in brief": when memory runs out a sequence can be
+ * preempted by swapping its blocks to CPU memory and back later; "Serving:
+ * vLLM and PagedAttention" names the same swap. Swap-out copies device
+ * blocks to host blocks, swap-in copies them back, possibly under other
+ * ids; the allocator's bookkeeping (which ids, the tables) is the caller's.
+ *
+ * For each pair p: block pairs[p][1] of (dst_k, dst_v) becomes a byte copy
+ * of block pairs[p][0] of (src_k, src_v). A block is block_bytes bytes
+ * (n_kv_heads * block_size * head_dim * element size; a multiple of 16), so
+ * the call serves bf16 and fp8 pools alike. A pair with an id outside
+ * [0, src_num_blocks) or [0, dst_num_blocks) is skipped and flagged
+ * PA_DEV_ERR_PAIR. Destination ids must be distinct.
+ *
+ * Every pointer (the four pools, pairs and err_word) must be memory this
+ * device can address: its own device memory, managed memory, or page-locked
+ * host memory (cudaHostAlloc / cudaMallocHost / registered), which the
+ * kernel reads or writes directly through its mapped address. Anything else
+ * (pageable host memory, another device's memory) returns
+ * PA_ERR_INVALID_ARG before anything is launched. The kernel is ordered on
+ * `stream` like the other calls; host memory it writes is complete once the
+ * stream has reached the call.
+ */
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                         const int32_t* pairs, int n_pairs, size_t block_bytes,
+                         int src_num_blocks, int dst_num_blocks, int32_t* err_word,
+                         pa_stream_t stream);
+
+/*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device
  * memory. The paper has no counterpart; this is a library convenience.
  *

@@ -43,6 +43,7 @@ SIGNATURES = {
     "pa_reshape_and_cache_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, C.c_float,
                                       C.c_float, _vp, _vp]),
     "pa_copy_blocks_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "pa_swap_blocks": (_i, [_vp, _vp, _vp, _vp, _vp, _i, C.c_size_t, _i, _i, _vp, _vp]),
     "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
                            C.c_float, C.c_float, _i, _vp, C.c_size_t, _vp, _vp]),
 }
@@ -308,3 +309,42 @@ def pa_decode_fp8(out, q, k_pool, v_pool, block_tables, seq_lens, scale, k_scale
     if st != PA_OK:
         raise PAError("pa_decode_fp8", st)
     return out
+
+
+# ------------------------------------------------------------------ swap
+
+def _check_pool_any(t, name, like=None):
+    """A contiguous pool tensor on the GPU or in page-locked host memory."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or page-locked (pinned) host memory")
+    if like is not None and (t.dtype != like.dtype or t.shape[1:] != like.shape[1:]):
+        raise ValueError(f"{name} blocks must have the dtype and shape of the other pool's")
+
+
+def pa_swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, err_word=None, stream=None):
+    """Block pairs[p, 1] of (dst_k, dst_v) becomes a copy of block pairs[p, 0]
+    of (src_k, src_v); either pool pair may live in pinned host memory (the
+    kernel reads or writes it directly). Swap-out: device pools -> host
+    pools; swap-in: back."""
+    _check_pool_any(src_k, "src_k")
+    _check_pool_any(src_v, "src_v", src_k)
+    _check_pool_any(dst_k, "dst_k", src_k)
+    _check_pool_any(dst_v, "dst_v", src_k)
+    if src_v.shape != src_k.shape or dst_v.shape != dst_k.shape:
+        raise ValueError("K and V pools of one side must match")
+    _check(pairs, "pairs", torch.int32, 2)
+    dev = pairs.device
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    if pairs.numel() and pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2]")
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    st = lib().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v), _ptr(pairs),
+                              pairs.shape[0], block_bytes, src_k.shape[0], dst_k.shape[0],
+                              _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_swap_blocks", st)

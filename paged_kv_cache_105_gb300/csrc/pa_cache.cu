@@ -122,6 +122,62 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restric
   }
 }
 
+// Swap: grid.y strides over pairs; threads stride over the 16-byte chunks of
+// the K block then the V block. Either side may be host memory the device
+// addresses directly (pinned and mapped), so the copy runs over the
+// chip-to-chip link without staging or one copy call per block.
+__global__ void __launch_bounds__(256)
+swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                   const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                   const int32_t* __restrict__ pairs, int n_pairs, int src_num_blocks,
+                   int dst_num_blocks, int64_t chunks_per_block, int32_t* err) {
+  for (int p = blockIdx.y; p < n_pairs; p += gridDim.y) {
+    const int32_t src = pairs[2 * p];
+    const int32_t dst = pairs[2 * p + 1];
+    if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) report(err, PA_DEV_ERR_PAIR);
+      continue;
+    }
+    const int64_t total = 2 * chunks_per_block;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+      const bool is_v = i >= chunks_per_block;
+      const int64_t c = is_v ? i - chunks_per_block : i;
+      const uint4 val = (is_v ? src_v : src_k)[(int64_t)src * chunks_per_block + c];
+      (is_v ? dst_v : dst_k)[(int64_t)dst * chunks_per_block + c] = val;
+    }
+  }
+}
+
+// The address through which the current device reaches `p`: device or
+// managed memory of this device as is, page-locked host memory through its
+// mapped device pointer. Anything else (pageable host memory, another
+// device's memory) is refused before a kernel could touch it.
+static bool device_view(const void* p, const void** out) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the failed query recorded
+    return false;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+      if (at.device != dev) return false;
+      *out = p;
+      return true;
+    case cudaMemoryTypeManaged:
+      *out = p;
+      return true;
+    case cudaMemoryTypeHost:
+      if (at.devicePointer == nullptr) return false;
+      *out = at.devicePointer;
+      return true;
+    default:
+      return false;
+  }
+}
+
 static bool supported_dims(int head_dim, int block_size) {
   return (head_dim == 64 || head_dim == 128) &&
          (block_size == 8 || block_size == 16 || block_size == 32);
@@ -225,4 +281,35 @@ extern "C" pa_status pa_copy_blocks_fp8(void* k_pool, void* v_pool, const int32_
       (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks_fp8 launch", e);
+}
+
+extern "C" pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k,
+                                    const void* src_v, const int32_t* pairs, int n_pairs,
+                                    size_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                                    int32_t* err_word, pa_stream_t stream) {
+  if (n_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (block_bytes == 0 || block_bytes % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!dst_k || !dst_v || !src_k || !src_v || !pairs) return PA_ERR_INVALID_ARG;
+  const void* ptr[5] = {dst_k, dst_v, src_k, src_v, pairs};
+  const void* dv[5];
+  for (int i = 0; i < 5; ++i)
+    if (!device_view(ptr[i], &dv[i])) return PA_ERR_INVALID_ARG;
+  if (err_word) {
+    const void* ew;
+    if (!device_view(err_word, &ew)) return PA_ERR_INVALID_ARG;
+    err_word = const_cast<int32_t*>(static_cast<const int32_t*>(ew));
+  }
+  for (int i = 0; i < 4; ++i)
+    if (!aligned16(dv[i])) return PA_ERR_INVALID_ARG;
+  const int64_t chunks = (int64_t)(block_bytes / 16);
+  const int threads = 256;
+  int64_t bx = (2 * chunks + threads - 1) / threads;
+  if (bx > 16) bx = 16;
+  const unsigned gy = (unsigned)(n_pairs < 65535 ? n_pairs : 65535);
+  swap_blocks_kernel<<<dim3((unsigned)bx, gy), threads, 0, (cudaStream_t)stream>>>(
+      (uint4*)dv[0], (uint4*)dv[1], (const uint4*)dv[2], (const uint4*)dv[3],
+      (const int32_t*)dv[4], n_pairs, src_num_blocks, dst_num_blocks, chunks, err_word);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_swap_blocks launch", e);
 }
