@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32])
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--e2e-steps", type=int, default=None)
@@ -219,6 +219,8 @@ def run_reference(args):
     if rank != 0:
         return
     wl = build_workload(args.config, args.block_size)
+    if hasattr(wl, "steps"):  # multi-step workload: the oracle times its first step
+        wl = wl.steps[0]
     budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
     seqs, tok = cpu_sample_seqs(wl, budget)
     fp8 = fp8_scale_of(args)
@@ -389,99 +391,120 @@ def main():
     from paged_kv_cache_105_gb300 import binding as B
     from paged_kv_cache_105_gb300 import workloads as W
 
-    wl = build_workload(args.config, args.block_size)
+    # A workload is a list of decode steps over one pool: one step for the
+    # single-step batches, T steps (forks, frees, copy-on-write between them)
+    # for beam search; the timed steps cycle through them.
+    wl0 = build_workload(args.config, args.block_size)
+    multi = isinstance(wl0, W.MultiStep)
+    steps_wl = wl0.steps if multi else [wl0]
+    wl = steps_wl[0]
+    name = wl0.name
+    T = len(steps_wl)
     fp8 = fp8_scale_of(args)
     P = wl.partition_tokens if args.partition_tokens is None else args.partition_tokens
     if fp8 is not None:
         P = 0  # the fp8 decode always runs the balanced split
-    P_res = B.pa_decode_partition_tokens(wl.num_seqs, wl.n_kv_heads, wl.block_size,
-                                         wl.max_seq_len, P)
+    msl = max(w.max_seq_len for w in steps_wl)
+    P_res = B.pa_decode_partition_tokens(wl.num_seqs, wl.n_kv_heads, wl.block_size, msl, P)
     eb = 1 if fp8 is not None else 2  # bytes per cached element
     base = W.make_values_fp8(wl, device=dev) if fp8 is not None else W.make_values(wl, device=dev)
+    step_vals = ([{k: base[k] for k in ("q", "k_new", "v_new")}] if not multi else
+                 [W.make_step_values(w, device=dev) for w in steps_wl])
+    pools0 = {k: base[k] for k in ("k_pool", "v_pool")}
     pool_bytes = 2 * base["k_pool"].numel() * eb
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    replicas = max(1, math.ceil(3 * l2 / max(1, wl.kv_bytes(eb))))
+    kv_min = min(w.kv_bytes(eb) for w in steps_wl)
+    replicas = 1 if multi else max(1, math.ceil(3 * l2 / max(1, kv_min)))
     replicas = min(replicas, max(1, int(40e9 // max(1, pool_bytes))))
-    reps = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(replicas - 1)]
-    t = {"bt": torch.from_numpy(wl.block_tables).to(dev),
-         "sl": torch.from_numpy(wl.seq_lens).to(dev),
-         "sm": torch.from_numpy(wl.slot_mapping).to(dev),
-         "pairs": torch.from_numpy(np.ascontiguousarray(wl.cow_pairs.reshape(-1, 2))).to(dev)}
-    outs = [torch.empty_like(r["q"]) for r in reps]
+    reps = [pools0] + [{k: v.clone() for k, v in pools0.items()} for _ in range(replicas - 1)]
+    maxw = max(w.block_tables.shape[1] for w in steps_wl)
+
+    def idx_tensors(w, to):
+        bt = np.full((w.num_seqs, maxw), W.PAD, np.int32)
+        bt[:, :w.block_tables.shape[1]] = w.block_tables
+        return {"bt": to(bt), "sl": to(w.seq_lens), "sm": to(w.slot_mapping),
+                "pairs": to(np.ascontiguousarray(w.cow_pairs.reshape(-1, 2)))}
+
+    tix = [idx_tensors(w, lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev))
+           for w in steps_wl]
+    outs = [torch.empty_like(base["q"]) for _ in reps]
     wss = [B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
-                              wl.block_size, wl.max_seq_len, P, device=dev) for _ in reps]
+                              wl.block_size, msl, P, device=dev) for _ in reps]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    n_pairs = int(wl.cow_pairs.shape[0])
-    max_parts = 1 if P == 0 else -(-max(1, wl.max_seq_len) // P)
-    launches_per_step = ((1 if n_pairs else 0) + (1 if wl.num_seqs else 0)
-                         + (1 if wl.num_seqs else 0) + (1 if (P == 0 or max_parts > 1) else 0))
+    npairs = [int(w.cow_pairs.shape[0]) for w in steps_wl]
+    max_parts = 1 if P == 0 else -(-max(1, msl) // P)
+    merge = 1 if (P == 0 or max_parts > 1) else 0
+    launches = [(1 if npairs[k] else 0) + 2 + merge for k in range(T)]
     stream = torch.cuda.current_stream(dev)
 
-    def api_write(r, pairs, k_new, v_new, sm):
+    def api_write(r, k, pairs, k_new, v_new, sm):
         if fp8 is not None:
-            if n_pairs:
+            if npairs[k]:
                 B.pa_copy_blocks_fp8(r["k_pool"], r["v_pool"], pairs, err_word=err)
             B.pa_reshape_and_cache_fp8(k_new, v_new, r["k_pool"], r["v_pool"], sm, fp8, fp8,
                                        err_word=err)
             return
-        if n_pairs:
+        if npairs[k]:
             B.pa_copy_blocks(r["k_pool"], r["v_pool"], pairs, err_word=err)
         B.pa_reshape_and_cache(k_new, v_new, r["k_pool"], r["v_pool"], sm, err_word=err)
 
     def api_decode(out, q, r, bt, sl, ws):
         if fp8 is not None:
             B.pa_decode_fp8(out, q, r["k_pool"], r["v_pool"], bt, sl, wl.scale, fp8, fp8,
-                            max_seq_len=wl.max_seq_len, workspace=ws, err_word=err)
+                            max_seq_len=msl, workspace=ws, err_word=err)
         else:
-            B.pa_decode(out, q, r["k_pool"], r["v_pool"], bt, sl, wl.scale,
-                        max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=P,
-                        err_word=err)
+            B.pa_decode(out, q, r["k_pool"], r["v_pool"], bt, sl, wl.scale, max_seq_len=msl,
+                        workspace=ws, partition_tokens=P, err_word=err)
 
-    def calls_write(r):
-        api_write(r, t["pairs"], r["k_new"], r["v_new"], t["sm"])
+    def calls_write(j, k):
+        sv, ti = step_vals[k], tix[k]
+        api_write(reps[j], k, ti["pairs"], sv["k_new"], sv["v_new"], ti["sm"])
 
-    def calls_decode(j):
-        r = reps[j]
-        api_decode(outs[j], r["q"], r, t["bt"], t["sl"], wss[j])
+    def calls_decode(j, k):
+        ti = tix[k]
+        api_decode(outs[j], step_vals[k]["q"], reps[j], ti["bt"], ti["sl"], wss[j])
+
+    def which(i):
+        return i % replicas, i % T
 
     # Eager warm-up (also the library's one-time set-up), then, unless
-    # --eager, one CUDA graph per replica for the writes and one for the
-    # decode, as a serving engine replays its decode step.
-    for j in range(replicas):
-        calls_write(reps[j])
-        calls_decode(j)
+    # --eager, CUDA graphs per (replica, step): the whole step (the decode is
+    # a programmatic dependent of the cache write, so their launches overlap)
+    # and the decode alone, as a serving engine replays its decode step.
+    for i in range(replicas * T):
+        calls_write(*which(i))
+        calls_decode(*which(i))
     torch.cuda.synchronize()
     graphs = None
     if not args.eager:
-        # per replica: the whole step (the decode is a programmatic dependent
-        # of the cache write, so their launches overlap) and the decode alone
-        graphs = []
+        graphs = {}
         cap = torch.cuda.Stream(dev)
         for j in range(replicas):
-            gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs, stream=cap):
-                calls_write(reps[j])
-                calls_decode(j)
-            with torch.cuda.graph(gd, stream=cap):
-                calls_decode(j)
-            graphs.append((gs, gd))
+            for k in range(T):
+                gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, stream=cap):
+                    calls_write(j, k)
+                    calls_decode(j, k)
+                with torch.cuda.graph(gd, stream=cap):
+                    calls_decode(j, k)
+                graphs[(j, k)] = (gs, gd)
         torch.cuda.synchronize()
 
     def step(i, ev=None):
-        j = i % replicas
+        j, k = which(i)
         if graphs is not None:
-            graphs[j][0].replay()
+            graphs[(j, k)][0].replay()
             return
-        calls_write(reps[j])
+        calls_write(j, k)
         if ev is not None:
             ev[0].record(stream)
-        calls_decode(j)
+        calls_decode(j, k)
         if ev is not None:
             ev[1].record(stream)
 
     def decode_only(i, ev):
         ev[0].record(stream)
-        graphs[i % replicas][1].replay()
+        graphs[which(i)][1].replay()
         ev[1].record(stream)
 
     def barrier():
@@ -532,48 +555,44 @@ def main():
 
     total_ms = t0.elapsed_time(t1)
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
     if world > 1:
         import torch.distributed as dist
         tt = torch.tensor([total_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
 
-    kv_bytes = wl.kv_bytes(eb)
-    alg_bytes = kv_bytes + wl.io_bytes()
+    timed = [steps_wl[i % T] for i in range(args.steps)]
+    kv_total = sum(w.kv_bytes(eb) for w in timed)
+    alg_total = sum(w.kv_bytes(eb) + w.io_bytes() for w in timed)
+    kv_bytes = kv_total / args.steps
+    alg_bytes = alg_total / args.steps
+    tok_total = sum(w.tokens_attended for w in timed)
     ms_per_step = total_ms / args.steps
-    value = world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    tokens_per_s = world * wl.tokens_attended * args.steps / (total_ms * 1e-3)
+    value = world * kv_total / (total_ms * 1e-3) / 1e9
+    tokens_per_s = world * tok_total / (total_ms * 1e-3)
 
     # ---- end to end through the public API, host buffers, copies timed
     e2e_steps = args.e2e_steps or max(10, min(200, args.steps))
-    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-            for k, v in base.items() if k in ("q", "k_new", "v_new")}
-    for k in host:
-        host[k].copy_(base[k].cpu())
-    host_idx = {"bt": torch.from_numpy(wl.block_tables).pin_memory(),
-                "sl": torch.from_numpy(wl.seq_lens).pin_memory(),
-                "sm": torch.from_numpy(wl.slot_mapping).pin_memory(),
-                "pairs": torch.from_numpy(np.ascontiguousarray(
-                    wl.cow_pairs.reshape(-1, 2))).pin_memory()}
+    host_vals = [{k: v.cpu().pin_memory() for k, v in sv.items()} for sv in step_vals]
+    host_idx = [idx_tensors(w, lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory())
+                for w in steps_wl]
     host_out = torch.empty(base["q"].shape, dtype=torch.bfloat16, pin_memory=True)
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    dev_idx = {k: torch.empty_like(v, device=dev) for k, v in host_idx.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
-        sum(v.numel() * v.element_size() for v in host_idx.values())
-    d2h = host_out.numel() * host_out.element_size()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_vals[0].items()}
+    h2d_steps, d2h = [], host_out.numel() * host_out.element_size()
 
     def e2e_step(i):
-        r = reps[i % replicas]
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        for k in host_idx:
-            dev_idx[k].copy_(host_idx[k], non_blocking=True)
-        api_write(r, dev_idx["pairs"], dev_in["k_new"], dev_in["v_new"], dev_idx["sm"])
-        api_decode(outs[i % replicas], dev_in["q"], r, dev_idx["bt"], dev_idx["sl"],
-                   wss[i % replicas])
-        host_out.copy_(outs[i % replicas], non_blocking=True)
+        j, k = which(i)
+        dev_idx = {}
+        for key in host_vals[k]:
+            dev_in[key].copy_(host_vals[k][key], non_blocking=True)
+        for key, v in host_idx[k].items():
+            dev_idx[key] = v.to(dev, non_blocking=True)
+        api_write(reps[j], k, dev_idx["pairs"], dev_in["k_new"], dev_in["v_new"], dev_idx["sm"])
+        api_decode(outs[j], dev_in["q"], reps[j], dev_idx["bt"], dev_idx["sl"], wss[j])
+        host_out.copy_(outs[j], non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()  # the caller needs the result
+        return (sum(v.numel() * v.element_size() for v in host_vals[k].values()) +
+                sum(v.numel() * v.element_size() for v in host_idx[k].values()))
 
     for i in range(3):
         e2e_step(i)
@@ -581,7 +600,7 @@ def main():
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for i in range(e2e_steps):
-        e2e_step(i)
+        h2d_steps.append(e2e_step(i))
     w1 = time.perf_counter()
     barrier()
     e2e_s = w1 - w0
@@ -590,14 +609,15 @@ def main():
         tt = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_s = float(tt.item())
-    e2e_value = world * kv_bytes * e2e_steps / e2e_s / 1e9
+    e2e_value = world * sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)) / e2e_s / 1e9
+    h2d = sum(h2d_steps) / len(h2d_steps)
 
     if rank != 0:
         return
 
     peak, peak_kind = measured_peak()
-    achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name + ("-fp8" if fp8 is not None else ""))
+    achieved = alg_total / (sum(dec_ms) * 1e-3) / 1e9
+    traffic = recorded_traffic(name + ("-fp8" if fp8 is not None else ""))
     kname = ("split_kernel<fp8> (pa_decode_fp8) + merge_kernel" if fp8 is not None else
              "split_kernel (pa_decode, balanced split) + merge_kernel" if P == 0 else
              "decode_kernel (pa_decode, fixed partitions) + merge_kernel")
@@ -610,7 +630,7 @@ def main():
                            if args.eager else
                            f"CUDA events around each of {args.steps} decode-graph replays "
                            "right after the timed steps (same inputs, same replicas)"),
-                "decode_ms_avg": dec_avg_ms}
+                "decode_ms_avg": sum(dec_ms) / len(dec_ms)}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -629,38 +649,54 @@ def main():
         cdt = time.perf_counter() - c0
         cpu = {"value": nbytes / cdt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{len(seqs)} of {wl.num_seqs} sequences ({tok} tokens, all "
-                         f"{wl.n_q_heads} query heads) x {reps_cpu} repetitions, "
-                         f"{cdt:.1f} s, single thread"}
+                         f"{wl.n_q_heads} query heads){' of the first step' if multi else ''}"
+                         f" x {reps_cpu} repetitions, {cdt:.1f} s, single thread"}
 
+    unique = None
+    if multi:
+        unique = [u * 2 * wl.n_kv_heads * wl.block_size * wl.head_dim * eb
+                  for u in wl0.used_blocks]
+    config = {"workload": name, "kv_dtype": args.kv, "num_seqs": wl.num_seqs,
+              "tokens_attended": int(tok_total / args.steps), "n_q_heads": wl.n_q_heads,
+              "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+              "block_size": wl.block_size, "partition_tokens": P_res,
+              "cow_pairs": int(sum(npairs) / T), "kv_bytes_per_step": int(kv_bytes),
+              "l2": (f"inputs rotated over {replicas} replicas "
+                     f"({replicas * kv_min / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2)"
+                     if not multi else
+                     f"one pool; {kv_bytes / 1e6:.0f} MB of KV read per step (logical) over "
+                     f"{max(unique) / 1e6:.0f} MB of unique blocks vs {l2 / 1e6:.0f} MB L2: "
+                     "L2-assisted"),
+              "arithmetic": ("bf16 operands, fp32 accumulation and softmax"
+                             if fp8 is None else
+                             "E4M3 codes and q as f16 mma operands, fp32 accumulation "
+                             "and softmax; per-tensor scales"),
+              "launch": "eager calls from Python" if args.eager else
+                        "one CUDA graph replay per step (copy, write, decode, merge)",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if multi:
+        config["decode_steps"] = T
+        config["steps_cycle"] = (f"the timed steps cycle through the {T} precomputed beam "
+                                 "steps (forks, frees, copy-on-write) on one pool")
+        config["sharing"] = {"used_blocks_last": wl0.used_blocks[-1],
+                             "unshared_blocks_last": wl0.unshared_blocks[-1],
+                             "saving": 1 - wl0.used_blocks[-1] / wl0.unshared_blocks[-1]}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if fp8 is None else "e4m3 K/V, bf16 q/out",
         "data": "synthetic",
-        "config": {"workload": wl.name, "kv_dtype": args.kv, "num_seqs": wl.num_seqs,
-                   "tokens_attended": wl.tokens_attended, "n_q_heads": wl.n_q_heads,
-                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
-                   "block_size": wl.block_size, "partition_tokens": P_res,
-                   "cow_pairs": n_pairs, "kv_bytes_per_step": kv_bytes,
-                   "l2": f"inputs rotated over {replicas} replicas "
-                         f"({replicas * kv_bytes / 1e6:.0f} MB of KV vs {l2 / 1e6:.0f} MB L2)",
-                   "arithmetic": ("bf16 operands, fp32 accumulation and softmax"
-                                  if fp8 is None else
-                                  "E4M3 codes and q as f16 mma operands, fp32 accumulation "
-                                  "and softmax; per-tensor scales"),
-                   "launch": "eager calls from Python" if args.eager else
-                             "one CUDA graph replay per step (copy, write, decode, merge)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config,
         "tokens_attended_per_s": tokens_per_s,
         "pct_of_peak": 100.0 * value / peak,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "note": "pinned host inputs copied in, result copied out and synchronised "
                         "every step"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": sum(launches[i % T] for i in range(args.steps)),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

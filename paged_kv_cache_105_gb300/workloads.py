@@ -354,7 +354,102 @@ def custom(lens, *, block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128, seed
                    partition_tokens=partition_tokens)
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+@dataclass
+class MultiStep:
+    """Several decode steps over one pool. steps[t] is step t's Workload (the
+    tables, lengths, slots and copy-on-write pairs after that step's forks,
+    frees and appends); ops is the whole allocator log and op_end[t] the log
+    length after step t; used_blocks[t] counts pool blocks in use after step
+    t and unshared_blocks[t] what the same tables would take without
+    sharing (sum over sequences of ceil(len / block_size))."""
+    name: str
+    steps: list
+    ops: list
+    op_end: list
+    free_order: np.ndarray
+    num_blocks: int
+    used_blocks: list
+    unshared_blocks: list
+
+    @property
+    def block_size(self) -> int:
+        return self.steps[0].block_size
+
+
+def beam_search(*, requests: int = 16, beams: int = 8, steps: int = 32,
+                prompt_median: float = 1000.0, prompt_sigma: float = 0.5,
+                prompt_lo: int = 32, prompt_hi: int = 4096, keep: float = 0.7,
+                block_size: int = 16, Hq: int = 32, Hkv: int = 8, d: int = 128,
+                seed: int = 6, name: str = "") -> MultiStep:
+    """Beam search (or, with keep=1, parallel sampling) over a shared prompt.
+
+    Each request's prompt (lognormal length, seeded) is cached once; `beams`
+    sequences fork from it. Every step first re-selects the beams (from the
+    second step on): beam j keeps its own lineage with probability `keep`,
+    else it continues a uniformly drawn beam of the same request, so beams
+    diverge and re-converge at staggered times. The first child of a parent
+    continues the parent's sequence, further children fork it, parents with
+    no child are freed. Then every beam appends its new token; a token that
+    lands in a block shared with a sibling copies the block first. Sequences
+    are ordered (request, beam) in every step."""
+    rng = np.random.default_rng(seed)
+    P = _lognormal_lengths(rng, requests, prompt_median, prompt_sigma, prompt_lo, prompt_hi)
+    per_beam = -(-(P.astype(np.int64) + steps) // block_size)
+    nb = int(beams * per_beam.sum()) + beams * requests  # never exhausted
+    free_order = rng.permutation(nb)
+    tb = _Tables(free_order, block_size)
+    cur = []
+    for r in range(requests):
+        root = tb.add()
+        tb.grow(root, int(P[r]))
+        cur.append([root] + [tb.fork(root) for _ in range(beams - 1)])
+    name = name or (f"beam-search-{requests}x{beams}beams-prompt{int(prompt_median)}"
+                    f"-{steps}steps-keep{keep:g}-bs{block_size}-q{Hq}kv{Hkv}-d{d}")
+    out, op_end, used, unshared = [], [], [], []
+    for t in range(steps):
+        slots, pairs, seqs = [], [], []
+        for r in range(requests):
+            if t > 0:
+                parents = [j if rng.random() < keep else int(rng.integers(0, beams))
+                           for j in range(beams)]
+                taken, new = set(), []
+                for p in parents:
+                    if p in taken:
+                        new.append(tb.fork(cur[r][p]))
+                    else:
+                        taken.add(p)
+                        new.append(cur[r][p])
+                for p in range(beams):
+                    if p not in taken:
+                        tb.free(cur[r][p])
+                cur[r] = new
+            for sq in cur[r]:
+                slot, pair = tb.step(sq)
+                slots.append(slot)
+                seqs.append(sq)
+                if pair:
+                    pairs.append(pair)
+        out.append(_finish(f"{name}-step{t}", tb, seqs, free_order, Hq=Hq, Hkv=Hkv, d=d,
+                           num_blocks=nb, seed=seed * 1000 + t, slots=slots, pairs=pairs))
+        op_end.append(len(tb.ops))
+        used.append(len(tb.ref))
+        unshared.append(int(sum(-(-tb.lens[sq] // block_size) for sq in seqs)))
+    for w in out:
+        w.ops = []  # the log lives in the MultiStep
+    return MultiStep(name=name, steps=out, ops=list(tb.ops), op_end=op_end,
+                     free_order=np.asarray(free_order, np.int32), num_blocks=nb,
+                     used_blocks=used, unshared_blocks=unshared)
+
+
+def config6(seed: int = 6) -> MultiStep:
+    """Beam search: 16 requests x 8 beams over prompts of lognormal length
+    (median 1000, sigma 0.5, clipped to [32, 4096]), 32 decode steps, beams
+    keep their lineage with probability 0.7 per step; block 16, 32 q / 8 kv
+    heads, head_dim 128."""
+    return beam_search(seed=seed)
+
+
+CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5, 6: config6}
 
 
 # ------------------------------------------------------------------ values
@@ -409,6 +504,21 @@ def make_values(wl: Workload, device="cpu", seed=None, poison_tails: bool = Fals
                     view = out[name].view(torch.int16)
                     view[blk, :, start:, :] = bits - (1 << 16 if bits >= 1 << 15 else 0)
     return out
+
+
+def make_step_values(wl: Workload, device="cpu", seed=None):
+    """The per-step inputs alone (q, k_new, v_new; bf16 N(0, 1), seeded by the
+    step's workload): for multi-step runs whose pools persist across steps."""
+    import torch
+
+    seed = wl.seed if seed is None else seed
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + 41)
+    S, Hq, Hkv, d = wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    bf = torch.bfloat16
+    return {"q": torch.randn((S, Hq, d), generator=g, device=device, dtype=bf),
+            "k_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf),
+            "v_new": torch.randn((S, Hkv, d), generator=g, device=device, dtype=bf)}
 
 
 # fp8 (E4M3) cache contents. A full fp8 cache stands for K/V ~ N(0, 1) that
