@@ -267,6 +267,42 @@ extern "C" int paref_attention_paged(double* out, const uint16_t* q, const uint1
   return 0;
 }
 
+extern "C" int paref_prefill_paged(double* out, const uint16_t* q, const uint16_t* k_pool,
+                                   const uint16_t* v_pool, const int32_t* block_tables,
+                                   const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                                   int max_blocks, int num_blocks, int n_q_heads, int n_kv_heads,
+                                   int head_dim, int block_size, double scale,
+                                   const int32_t* rows, int n_rows) {
+  if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0 || num_seqs < 0) return -1;
+  const int group = n_q_heads / n_kv_heads;
+  const int total_q = num_seqs > 0 ? cu_q[num_seqs] : 0;
+  const int64_t total = rows ? n_rows : (int64_t)total_q * n_q_heads;
+  for (int64_t r = 0; r < total; ++r) {
+    const int row = rows ? rows[2 * r] : (int)(r / n_q_heads);
+    const int h = rows ? rows[2 * r + 1] : (int)(r % n_q_heads);
+    if (row < 0 || row >= total_q || h < 0 || h >= n_q_heads) return -1;
+    int s = 0;  // the sequence whose chunk holds this query row
+    while (s + 1 < num_seqs && cu_q[s + 1] <= row) ++s;
+    const int c = cu_q[s + 1] - cu_q[s];
+    const int len = seq_lens[s];
+    if (c < 0 || len < c || (int64_t)len > (int64_t)max_blocks * block_size) return -1;
+    const int pos = len - c + (row - cu_q[s]);  // this query token's position
+    const int g = h / group;
+    std::vector<const uint16_t*> keys(pos + 1), vals(pos + 1);
+    for (int j = 0; j <= pos; ++j) {
+      const int32_t phys = block_tables[(int64_t)s * max_blocks + j / block_size];
+      if (phys < 0 || phys >= num_blocks) return -1;
+      const int64_t off =
+          (((int64_t)phys * n_kv_heads + g) * block_size + j % block_size) * head_dim;
+      keys[j] = k_pool + off;
+      vals[j] = v_pool + off;
+    }
+    attend_row(out + r * head_dim, q + ((int64_t)row * n_q_heads + h) * head_dim, keys, vals,
+               head_dim, scale);
+  }
+  return 0;
+}
+
 extern "C" int paref_attention_contiguous(double* out, const uint16_t* q, const uint16_t* k,
                                           const uint16_t* v, int len, int n_q_heads,
                                           int n_kv_heads, int head_dim, double scale) {

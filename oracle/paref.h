@@ -109,6 +109,28 @@ int paref_attention_contiguous(double* out, const uint16_t* q, const uint16_t* k
                                const uint16_t* v, int len, int n_q_heads, int n_kv_heads,
                                int head_dim, double scale);
 
+/* ---------------- chunked prefill ("Serving: vLLM and PagedAttention",
+   section 2.4, chunked prefill: a prompt is split into chunks that run
+   beside decode steps; each chunk's tokens attend, causally, to everything
+   cached before them and to the chunk's earlier tokens) ---------------- */
+
+/* Sequence s contributes c_s = cu_q[s+1] - cu_q[s] query tokens (rows
+   cu_q[s] .. cu_q[s+1]-1 of q and out, [total_q][n_q_heads][head_dim]),
+   which are its LAST c_s tokens: seq_lens[s] counts everything cached,
+   the chunk included. Query token i of s sits at position
+   p = seq_lens[s] - c_s + i and attends to positions 0..p:
+     out[cu_q[s]+i, h, :] = sum_{j<=p} softmax_j(scale * q . K_j) V_j
+   with K_j, V_j gathered through the block table as for decode. When
+   rows != NULL only the listed (query row, head) pairs are computed, into
+   out[n_rows][head_dim]. Returns 0, or -1 on a bad table, length or
+   c_s > seq_lens[s]. */
+int paref_prefill_paged(double* out, const uint16_t* q, const uint16_t* k_pool,
+                        const uint16_t* v_pool, const int32_t* block_tables,
+                        const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                        int max_blocks, int num_blocks, int n_q_heads, int n_kv_heads,
+                        int head_dim, int block_size, double scale, const int32_t* rows,
+                        int n_rows);
+
 /* ---------------- cache writes ([P2] decode-step diagram: the new K and V
    go into the current block; copy-on-write diagram: copy, then write) ----- */
 

@@ -59,6 +59,9 @@ def lib():
                                                       C.c_int, C.c_int, C.c_int, C.c_int]),
                 "paref_copy_blocks": (C.c_int, [u16p, u16p, i32p, C.c_int, C.c_int, C.c_int,
                                                 C.c_int, C.c_int]),
+                "paref_prefill_paged": (C.c_int, [f64p, u16p, u16p, u16p, i32p, i32p, i32p,
+                                                  C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                                  C.c_int, C.c_int, C.c_double, i32p, C.c_int]),
                 "paref_swap_blocks": (C.c_int, [u8p, u8p, u8p, u8p, i32p, C.c_int, C.c_int64,
                                                 C.c_int, C.c_int]),
                 "paref_e4m3_decode": (C.c_double, [C.c_uint8]),
@@ -277,6 +280,35 @@ def copy_blocks(k_pool, v_pool, pairs) -> int:
     pr, prp = _i32(np.asarray(pairs).reshape(-1, 2))
     NB, Hkv, bs, d = k_pool.shape
     return lib().paref_copy_blocks(kpp, vpp, prp, pr.shape[0], Hkv, d, bs, NB)
+
+
+# ----------------------------------------------------------------- prefill
+
+def prefill_paged(q, k_pool, v_pool, block_tables, seq_lens, cu_q, scale, rows=None):
+    """Causal attention of each sequence's last c_s tokens (its chunk, rows
+    cu_q[s]..cu_q[s+1]-1 of q) over its whole cached context, in fp64."""
+    q, qp = _u16(q)
+    k_pool, kp = _u16(k_pool)
+    v_pool, vp = _u16(v_pool)
+    bt, btp = _i32(block_tables)
+    sl, slp = _i32(seq_lens)
+    cu, cup = _i32(cu_q)
+    TQ, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_pool.shape
+    S = len(sl)
+    assert d2 == d and len(cu) == S + 1 and int(cu[-1]) == TQ
+    if rows is None:
+        out = np.zeros((TQ, Hq, d), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        r, rp = _i32(np.asarray(rows).reshape(-1, 2))
+        nr = r.shape[0]
+        out = np.zeros((nr, d), dtype=np.float64)
+    rc = lib().paref_prefill_paged(out.ctypes.data_as(f64p), qp, kp, vp, btp, slp, cup, S,
+                                   bt.shape[1], NB, Hq, Hkv, d, bs, float(scale), rp, nr)
+    if rc != 0:
+        raise ValueError("oracle prefill: invalid table, length or chunk")
+    return out
 
 
 # ----------------------------------------------------------------- swap
