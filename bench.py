@@ -51,9 +51,9 @@ def parse():
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["decode", "swap"], default="decode",
+    p.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                    help="decode: the decode step (default); swap: block swap-out to pinned "
-                        "host memory and swap-in back")
+                        "host memory and swap-in back; prefill: a chunked-prefill step")
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales)")
     p.add_argument("--eager", action="store_true",
@@ -370,6 +370,107 @@ def run_swap(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args):
+    """One chunked-prefill step = the chunk tokens' cache write + causal
+    attention of every chunk token over its whole paged context. Metric:
+    causal attention flops per second (4 * head_dim * query heads per visible
+    (token, position) pair) against the measured bf16 tensor peak."""
+    import numpy as np
+    import torch
+    world, rank, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_105_gb300 import binding as B
+    from paged_kv_cache_105_gb300 import workloads as W
+    wl = W.prefill_chunked()
+    vals = W.make_prefill_values(wl, device=dev)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).to(dev)
+         for k in ("block_tables", "seq_lens", "cu_q", "slot_mapping")}
+    out = torch.empty_like(vals["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def write():
+        B.pa_reshape_and_cache(vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"],
+                               t["slot_mapping"], err_word=err)
+
+    def attend():
+        B.pa_prefill(out, vals["q"], vals["k_pool"], vals["v_pool"], t["block_tables"],
+                     t["seq_lens"], t["cu_q"], wl.scale, max_q_len=wl.max_q_len, err_word=err)
+
+    write()
+    attend()
+    torch.cuda.synchronize()
+    gs, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.graph(gs, stream=cap):
+        write()
+        attend()
+    with torch.cuda.graph(ga, stream=cap):
+        attend()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        gs.replay()
+    torch.cuda.synchronize()
+    t_pre = time.perf_counter()
+    while time.perf_counter() - t_pre < 1.0:
+        gs.replay()
+        torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        gs.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a_, b_ in evs:
+        a_.record(stream)
+        ga.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+    if rank != 0:
+        return
+    step_ms = e0.elapsed_time(e1) / args.steps
+    att_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
+    flops = wl.flops()
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    achieved = flops / (att_ms * 1e-3) / 1e12
+    peak, kind = None, "fallback"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peak = json.load(f).get("bf16_tflops")
+            kind = "measured"
+    if not peak:
+        peak = 1900.0
+    line = {"metric": "chunked-prefill causal attention TFLOP/s", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "batched_tokens": wl.total_q,
+                       "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
+                       "head_dim": wl.head_dim, "block_size": wl.block_size,
+                       "flops_per_step": flops, "kv_bytes": wl.kv_bytes(),
+                       "arithmetic": "bf16 mma.sync m16n8k16, fp32 accumulation; P as a "
+                                     "bf16 hi + lo pair, so the P V product runs twice",
+                       "launch": "one CUDA graph replay per step (write, prefill)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "kernel": "prefill_kernel (pa_prefill)",
+                         "peak_source": f"{kind} bf16_tflops (cuBLAS, burst)",
+                         "prefill_ms_avg": att_ms},
+            "gpu_launches": 2 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -377,6 +478,9 @@ def main():
         return
     if args.op == "swap":
         run_swap(args)
+        return
+    if args.op == "prefill":
+        run_prefill(args)
         return
 
     import numpy as np

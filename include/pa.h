@@ -168,6 +168,43 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     int32_t* err_word, pa_stream_t stream);
 
 /*
+ * pa_prefill — chunked-prefill attention over the paged cache.
+ * Defined by "Serving: vLLM and PagedAttention", section 2.4 (chunked
+ * prefill: a long prompt is processed in chunks that share steps with
+ * decodes) together with the paged gather of "03 · PagedAttention", "The
+ * part the analogy hides: the kernel". The chunk's own K/V are written to
+ * the pool first (pa_reshape_and_cache with one slot per chunk token).
+ *
+ * Sequence s contributes c_s = cu_q[s+1] - cu_q[s] query tokens, rows
+ * cu_q[s] .. cu_q[s+1]-1 of q and out, which are its LAST c_s tokens:
+ * seq_lens[s] counts every cached token, the chunk included. Query token i
+ * of s is at position p = seq_lens[s] - c_s + i and, for query head h with
+ * kv head g = h / G,
+ *   out[cu_q[s]+i][h][:] = sum_{j <= p} softmax_j(scale * q . K_j) V_j
+ * with K_j = k_pool[block_tables[s][j / block_size]][g][j % block_size][:].
+ * c_s = 1 for every s is decode; cu_q[s] = 0 history (seq_lens = c_s) is a
+ * whole-prompt prefill.
+ *
+ *   out            bf16 [cu_q[num_seqs]][n_q_heads][head_dim]
+ *   q              bf16 [cu_q[num_seqs]][n_q_heads][head_dim]
+ *   cu_q           int32 [num_seqs + 1], non-decreasing, cu_q[0] = 0 (device)
+ *   max_q_len      host bound of max_s c_s (sizes the grid); rows of a
+ *                  longer chunk are not written and PA_DEV_ERR_SEQ_LEN is set
+ *   n_q_heads / n_kv_heads  <= 64
+ *   others         as pa_decode (head_dim 64/128, block_size 8/16/32)
+ * seq_lens[s] > max_blocks_per_seq * block_size is clamped and flagged
+ * PA_DEV_ERR_SEQ_LEN; c_s > seq_lens[s] is flagged and that sequence's rows
+ * are not written. Bad block ids are skipped (their tokens weigh zero) and
+ * flagged PA_DEV_ERR_BLOCK_ID. No workspace. Launched as a programmatic
+ * dependent of the preceding kernel; it waits for it before reading.
+ */
+pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, const int32_t* seq_lens, const int32_t* cu_q,
+                     int num_seqs, int max_blocks_per_seq, int num_blocks, int n_q_heads,
+                     int n_kv_heads, int head_dim, int block_size, float scale, int max_q_len,
+                     int32_t* err_word, pa_stream_t stream);
+
+/*
  * pa_reshape_and_cache — write new tokens' K/V into their pool slots.
  * Defined by the "A DECODE STEP" diagram of "PagedAttention"
  * (mlapandio.dev): the step writes the new K and V into the sequence's

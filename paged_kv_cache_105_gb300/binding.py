@@ -43,6 +43,8 @@ SIGNATURES = {
     "pa_reshape_and_cache_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, C.c_float,
                                       C.c_float, _vp, _vp]),
     "pa_copy_blocks_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                        C.c_float, _i, _vp, _vp]),
     "pa_swap_blocks": (_i, [_vp, _vp, _vp, _vp, _vp, _i, C.c_size_t, _i, _i, _vp, _vp]),
     "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
                            C.c_float, C.c_float, _i, _vp, C.c_size_t, _vp, _vp]),
@@ -308,6 +310,37 @@ def pa_decode_fp8(out, q, k_pool, v_pool, block_tables, seq_lens, scale, k_scale
                              _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_decode_fp8", st)
+    return out
+
+
+# ------------------------------------------------------------------ prefill
+
+def pa_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q, scale, *, max_q_len,
+               err_word=None, stream=None):
+    """Causal attention of each sequence's chunk (its last cu_q[s+1]-cu_q[s]
+    tokens, rows cu_q[s].. of q) over its whole paged context (include/pa.h)."""
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    _check(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _check(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _check(block_tables, "block_tables", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _check(cu_q, "cu_q", torch.int32, 1, dev)
+    if err_word is not None:
+        _check(err_word, "err_word", torch.int32, None, dev)
+    TQ, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    S = seq_lens.shape[0]
+    if tuple(out.shape) != (TQ, Hq, D) or D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.shape[0] != S or cu_q.shape[0] != S + 1:
+        raise ValueError("block_tables needs one row and cu_q one entry per sequence (+1)")
+    st = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                          _ptr(seq_lens), _ptr(cu_q), S, block_tables.shape[1], NB, Hq, Hkv, D,
+                          bs, float(scale), int(max_q_len), _ptr(err_word), _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_prefill", st)
     return out
 
 

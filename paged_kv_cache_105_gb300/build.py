@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu"]
+SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

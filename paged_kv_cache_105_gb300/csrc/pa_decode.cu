@@ -1397,8 +1397,8 @@ static pa_status encode_pool_map(CUtensorMap* map, const void* pool, int D, int 
 
 // Encoding a tensor map costs host time on every call; a decode loop reuses
 // the same pools, so keep the last few per thread.
-static pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int eb, int64_t rows,
-                               int box_rows, bool try3d, int* map3d) {
+pa_status make_pool_map(CUtensorMap* map, const void* pool, int D, int eb, int64_t rows,
+                        int box_rows, bool try3d, int* map3d) {
   struct Entry {
     const void* pool;
     int D, eb, box_rows, try3d, map3d;

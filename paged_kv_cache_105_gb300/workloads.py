@@ -355,6 +355,124 @@ def custom(lens, *, block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128, seed
 
 
 @dataclass
+class PrefillWorkload:
+    """One chunked-prefill step: sequence s has seq_lens[s] - chunk_lens[s]
+    cached tokens and appends a chunk of chunk_lens[s] tokens (rows
+    cu_q[s]..cu_q[s+1]-1 of the batch), whose K/V go to slot_mapping[row]."""
+    name: str
+    num_seqs: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    seq_lens: np.ndarray      # int32 [S], cached tokens after the chunk
+    chunk_lens: np.ndarray    # int32 [S]
+    cu_q: np.ndarray          # int32 [S + 1]
+    block_tables: np.ndarray  # int32 [S, max_blocks]
+    slot_mapping: np.ndarray  # int32 [total_q]
+    free_order: np.ndarray
+    ops: list = field(default_factory=list)
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_q[-1])
+
+    @property
+    def max_q_len(self) -> int:
+        return int(self.chunk_lens.max()) if self.num_seqs else 0
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.num_seqs else 0
+
+    @property
+    def group(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+    def visible_pairs(self) -> int:
+        """Sum over query tokens of the positions each attends to (p + 1)."""
+        tot = 0
+        for L, c in zip(self.seq_lens.astype(np.int64), self.chunk_lens.astype(np.int64)):
+            tot += c * (L - c) + c * (c + 1) // 2
+        return int(tot)
+
+    def flops(self) -> int:
+        """Causal attention flops: 2 (QK) + 2 (PV) multiply-adds of head_dim per
+        visible (query token, position) pair and query head."""
+        return 4 * self.head_dim * self.n_q_heads * self.visible_pairs()
+
+    def kv_bytes(self, elem_bytes: int = 2) -> int:
+        """K+V bytes of every cached position of every sequence, read once."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.n_kv_heads * \
+            self.head_dim * elem_bytes * 2
+
+
+def prefill_batch(contexts, chunks, *, block_size: int = 16, Hq: int = 32, Hkv: int = 8,
+                  d: int = 128, seed: int = 0, extra_blocks: int = 8,
+                  name: str = "") -> PrefillWorkload:
+    """Sequences with contexts[s] cached tokens each, then a chunk of
+    chunks[s] tokens per sequence, blocks handed out from a seeded shuffled
+    free list (history first, sequence by sequence, then the chunks)."""
+    rng = np.random.default_rng(seed)
+    ctx = [int(x) for x in contexts]
+    ch = [int(x) for x in chunks]
+    nb = sum(-(-(a + b) // block_size) for a, b in zip(ctx, ch)) + extra_blocks
+    free_order = rng.permutation(nb)
+    tb = _Tables(free_order, block_size)
+    seqs = [tb.add() for _ in ctx]
+    for sq, a in zip(seqs, ctx):
+        tb.grow(sq, a)
+    slots = []
+    for sq, a, b in zip(seqs, ctx, ch):
+        tb.grow(sq, b)
+        for pos in range(a, a + b):
+            slots.append(tb.tables[sq][pos // block_size] * block_size + pos % block_size)
+    lens = np.array([a + b for a, b in zip(ctx, ch)], np.int32)
+    maxb = max(1, max(len(tb.tables[sq]) for sq in seqs))
+    bt = np.full((len(seqs), maxb), PAD, np.int32)
+    for i, sq in enumerate(seqs):
+        bt[i, :len(tb.tables[sq])] = tb.tables[sq]
+    cu = np.concatenate([[0], np.cumsum(ch)]).astype(np.int32)
+    name = name or f"prefill-{len(ctx)}seq-q{Hq}kv{Hkv}-d{d}-bs{block_size}"
+    return PrefillWorkload(name=name, num_seqs=len(ctx), n_q_heads=Hq, n_kv_heads=Hkv,
+                           head_dim=d, block_size=block_size, num_blocks=nb, seq_lens=lens,
+                           chunk_lens=np.array(ch, np.int32), cu_q=cu, block_tables=bt,
+                           slot_mapping=np.array(slots, np.int32),
+                           free_order=np.asarray(free_order, np.int32), ops=tb.ops, seed=seed)
+
+
+def prefill_chunked(seed: int = 7) -> PrefillWorkload:
+    """A chunked-prefill step of 8192 batched tokens: eight 8192-token prompts,
+    each at a different chunk (chunk 1024 tokens, contexts 0, 1024, ..., 7168
+    already cached); block 16, 32 q / 8 kv heads, head_dim 128."""
+    return prefill_batch([1024 * k for k in range(8)], [1024] * 8, seed=seed,
+                         name="chunked-prefill-8x1024-ctx0to7168-bs16-q32kv8-d128")
+
+
+def make_prefill_values(wl: PrefillWorkload, device="cpu", seed=None):
+    """bf16 N(0, 1): q and the chunk's new K/V [total_q, ...], the pools."""
+    import torch
+
+    seed = wl.seed if seed is None else seed
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + 53)
+    TQ, Hq, Hkv, d, bs, NB = (wl.total_q, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                              wl.block_size, wl.num_blocks)
+    bf = torch.bfloat16
+    return {"q": torch.randn((TQ, Hq, d), generator=g, device=device, dtype=bf),
+            "k_new": torch.randn((TQ, Hkv, d), generator=g, device=device, dtype=bf),
+            "v_new": torch.randn((TQ, Hkv, d), generator=g, device=device, dtype=bf),
+            "k_pool": torch.randn((NB, Hkv, bs, d), generator=g, device=device, dtype=bf),
+            "v_pool": torch.randn((NB, Hkv, bs, d), generator=g, device=device, dtype=bf)}
+
+
+@dataclass
 class MultiStep:
     """Several decode steps over one pool. steps[t] is step t's Workload (the
     tables, lengths, slots and copy-on-write pairs after that step's forks,
