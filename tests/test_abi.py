@@ -124,3 +124,54 @@ def test_cache_calls_host_validation(L):
     assert L.pa_copy_blocks(p, p, p, 3, 2, 128, 4, 8, None, None) == UNS
     assert L.pa_copy_blocks(p, p, p, -2, 2, 128, 16, 8, None, None) == INV
     assert L.pa_copy_blocks(None, None, None, 0, 2, 128, 16, 8, None, None) == B.PA_OK
+
+
+@no_gpu
+def test_fp8_calls_host_validation(L):
+    INV, UNS = B.PA_ERR_INVALID_ARG, B.PA_ERR_UNSUPPORTED
+    p = 1 << 12
+    f = L.pa_decode_fp8
+
+    def dec(D=128, ks=0.01, vs=0.01, S=2, q=p):
+        return f(p, q, p, p, p, p, S, 4, 8, 8, 2, D, 16, 0.1, ks, vs, 64, 1 << 16, 1 << 20,
+                 None, None)
+
+    assert dec(D=64) == UNS                      # fp8 decode: head_dim 128 only
+    assert dec(ks=0.0) == INV
+    assert dec(vs=float("inf")) == INV
+    assert dec(ks=-1.0) == INV
+    assert dec(q=None) == INV
+    assert dec(S=0) == B.PA_OK
+    w = L.pa_reshape_and_cache_fp8
+    assert w(p, p, p, p, p, 4, 8, 2, 128, 16, 0.0, 1.0, None, None) == INV
+    assert w(p, p, p, p, p, 4, 8, 2, 80, 16, 1.0, 1.0, None, None) == UNS
+    assert w(None, None, None, None, None, 0, 8, 2, 128, 16, 1.0, 1.0, None, None) == B.PA_OK
+    c = L.pa_copy_blocks_fp8
+    assert c(None, p, p, 3, 2, 128, 16, 8, None, None) == INV
+    assert c(p, p, p, 3, 2, 128, 4, 8, None, None) == UNS
+    assert c(None, None, None, 0, 2, 128, 16, 8, None, None) == B.PA_OK
+
+
+@no_gpu
+def test_prefill_and_swap_host_validation(L):
+    INV, UNS = B.PA_ERR_INVALID_ARG, B.PA_ERR_UNSUPPORTED
+    p = 1 << 12
+    f = L.pa_prefill
+
+    def pre(q=p, cu=p, S=2, Hq=8, Hkv=2, D=128, bs=16, maxq=64):
+        return f(p, q, p, p, p, p, cu, S, 4, 8, Hq, Hkv, D, bs, 0.1, maxq, None, None)
+
+    assert pre(D=96) == UNS
+    assert pre(bs=12) == UNS
+    assert pre(Hq=130, Hkv=2) == UNS             # group of 65 > 64 rows per tile
+    assert pre(Hq=6, Hkv=4) == INV
+    assert pre(cu=None) == INV
+    assert pre(q=p + 2) == INV                   # misaligned
+    assert pre(S=0, q=None) == B.PA_OK
+    assert pre(maxq=0, q=None) == B.PA_OK
+    assert pre(maxq=-1) == INV
+    s = L.pa_swap_blocks
+    assert s(p, p, p, p, p, 2, 24, 4, 4, None, None) == INV        # block not 16-B multiple
+    assert s(p, p, p, p, p, -1, 1024, 4, 4, None, None) == INV
+    assert s(None, None, None, None, None, 0, 1024, 4, 4, None, None) == B.PA_OK
+    assert s(p, p, p, p, p, 1, 1024, 4, 4, None, None) == INV      # no device to address p
