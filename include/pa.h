@@ -191,6 +191,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  *   max_q_len      host bound of max_s c_s (sizes the grid); rows of a
  *                  longer chunk are not written and PA_DEV_ERR_SEQ_LEN is set
  *   n_q_heads / n_kv_heads  <= 64
+ *   scale          finite and > 0 (else PA_ERR_INVALID_ARG)
  *   others         as pa_decode (head_dim 64/128, block_size 8/16/32)
  * seq_lens[s] > max_blocks_per_seq * block_size is clamped and flagged
  * PA_DEV_ERR_SEQ_LEN; c_s > seq_lens[s] is flagged and that sequence's rows

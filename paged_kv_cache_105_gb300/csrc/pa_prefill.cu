@@ -1,4 +1,5 @@
-// Paged chunked-prefill attention for sm_103a.
+// Paged chunked-prefill attention for sm_103a, on the fifth-generation tensor
+// cores (tcgen05, accumulators in tensor memory).
 //
 // What it computes ("Serving: vLLM and PagedAttention", section 2.4, chunked
 // prefill; "03 · PagedAttention", the kernel gathers K/V through the block
@@ -6,17 +7,27 @@
 // each attend causally to every cached position up to their own, the pool
 // reached through the block table exactly as in decode.
 //
-// Design: one CTA per (query tile, sequence, kv head). The tile's rows are
-// (token, query head) pairs of the G query heads sharing the kv head, 64 rows
-// (64 / G tokens), 16 per warp, so every K/V unit staged in shared memory
-// serves all G heads. 16-token K/V units stream through a 4-stage ring filled
-// by TMA (128-byte swizzle, the same boxes as decode) and shared by the four
-// warps. Per unit and warp: S = Q K^T with Q in registers and K^T fragments
-// from ldmatrix, causal and length masking, online softmax in base 2 with a
-// lazily moved reference, then O += P V with P reused from the score
-// registers (as a bf16 hi + lo pair) and V^T fragments from ldmatrix.trans;
-// bf16 mma.sync m16n8k16, fp32 accumulation. Tiles are numbered so the longest (latest) tiles of a
-// sequence start first.
+// Design: one CTA (two warpgroups) per (query tile, sequence, kv head). The
+// tile is 256 rows of (token, query head) pairs of the G query heads sharing
+// the kv head (256 / G tokens), so every K/V tile in shared memory serves all
+// G heads twice over; each warpgroup owns 128 rows (one MMA M), and row r of
+// a warpgroup's accumulators is TMEM lane r, owned by its thread r: the
+// softmax of a row runs in one thread with no shuffles.
+//  * Q (2 x 128 x head_dim, bf16) is staged once in shared memory in the
+//    128-byte-swizzled K-major layout the MMA reads.
+//  * K/V stream in tiles of 64 tokens (four 16-token units, the decode's TMA
+//    boxes, each 64-column half of a row stored as its own 64-row slab)
+//    through a 3-stage ring filled by TMA.
+//  * Per tile: S = Q K^T (M 128, N 64, both operands K-major) into TMEM;
+//    every thread loads its row of S, masks it (causal, length, bad blocks),
+//    runs the online softmax in base 2 with a lazily moved reference
+//    (rescaling its row of O in TMEM in the rare case the reference moves),
+//    and writes P to shared memory as a bf16 pair hi + lo; then
+//    O += P_hi V + P_lo V (M 128, N head_dim, V read MN-major) accumulates in
+//    TMEM. One thread issues the MMAs; one mbarrier commit per tile covers
+//    the P V of this tile and the S of the next.
+//  * O is normalised and written as bf16 after the last tile.
+// Tiles are numbered so a sequence's latest (longest) tiles start first.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,19 +35,26 @@
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kPWarps = 4;
-constexpr int kPThreads = kPWarps * 32;
-constexpr int kPRows = kPWarps * 16;  // (token, head) rows per tile
-constexpr int kPUnit = 16;            // K/V tokens per stage
-constexpr int kPStages = 4;
-constexpr uint64_t kPWaitNs = 2000000000ull;      // 2 s: a wait that long is a fault
-constexpr uint64_t kPWaitAfterFaultNs = 1000000ull;
-constexpr float kPLazyLog2 = 8.f;
-constexpr float kPLog2e = 1.4426950408889634f;
+constexpr int kTWarpgroups = 2;             // each owns 128 rows (one MMA M)
+constexpr int kTThreads = 128 * kTWarpgroups;
+constexpr int kTRows = 128;                 // M of every MMA: rows per warpgroup
+constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
+constexpr int kTKv = 64;                    // K/V tokens per tile (N of S)
+constexpr int kTUnit = 16;                  // tokens per TMA unit
+constexpr int kTUnits = kTKv / kTUnit;
+constexpr int kTStages = 3;
+// TMEM columns: S of warpgroup w at 64 w, its O at 128 + 128 w
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 128;
+constexpr uint64_t kTWaitNs = 2000000000ull;      // 2 s: a wait that long is a fault
+constexpr uint64_t kTWaitAfterFaultNs = 1000000ull;
+constexpr float kTLazyLog2 = 8.f;
+constexpr float kTLog2e = 1.4426950408889634f;
 
 struct PrefillArgs {
   __nv_bfloat16* out;
@@ -46,50 +64,58 @@ struct PrefillArgs {
   const int32_t* cu_q;
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
-  int tile_tokens;  // query tokens per tile: 64 / G, rounded down
+  int tile_tokens;  // query tokens per tile: 256 / G, rounded down
   int n_tiles;      // grid.x: tiles of the longest chunk
-  int map3d;
+  int max_q_len;    // host bound of the chunk lengths
   float scale_log2;
 };
 
 template <int D, int BS>
-struct PCfg {
-  static constexpr int ROWS = BS < kPUnit ? BS : kPUnit;  // rows per TMA box
-  static constexpr int BOXES = kPUnit / ROWS;
-  static constexpr int KH = D / 64;                       // 128-byte halves of a row
-  static constexpr int BOX_BYTES = KH * ROWS * 128;
-  static constexpr int KV_BYTES = BOXES * BOX_BYTES;      // 16 rows of K (or V)
+struct TCfg {
+  static constexpr int ROWS = BS < kTUnit ? BS : kTUnit;  // rows per TMA box
+  static constexpr int BOXES = kTUnit / ROWS;             // boxes per unit
+  static constexpr int KH = D / 64;                       // 64-column halves
+  static constexpr int HALF = kTKv * 128;                 // one half of K (or V): 8 KB
+  static constexpr int KV_BYTES = KH * HALF;
   static constexpr int STAGE = 2 * KV_BYTES;
-  static constexpr int BAR_OFF = kPStages * STAGE;
-  static constexpr int MASK_OFF = BAR_OFF + kPStages * 8;
-  static constexpr int FAULT_OFF = MASK_OFF + kPStages * 4;
-  static constexpr size_t SMEM = 1024 + FAULT_OFF + 16;
+  static constexpr int QHALF = kTRows * 128;              // 16 KB
+  static constexpr int QWG = KH * QHALF;                  // one warpgroup's Q
+  static constexpr int Q_OFF = 0;
+  static constexpr int PBUF = kTRows * 128;
+  static constexpr int PWG = 2 * PBUF;                    // P hi, then P lo
+  static constexpr int P_OFF = Q_OFF + kTWarpgroups * QWG;
+  static constexpr int KV_OFF = P_OFF + kTWarpgroups * PWG;
+  static constexpr int BAR_OFF = KV_OFF + kTStages * STAGE;  // full[3], mma
+  static constexpr int MASK_OFF = BAR_OFF + (kTStages + 1) * 8;  // 64-bit token masks
+  static constexpr int TMEM_OFF = MASK_OFF + kTStages * 8;
+  static constexpr int FAULT_OFF = TMEM_OFF + 8;
+  static constexpr size_t SMEM = 1024 + FAULT_OFF + 8;
 };
 
-// Shared-memory address of 16-byte chunk `ch` of K/V row `r` (0..15) of a
-// unit staged at `base` (boxes of ROWS rows, 128-byte halves, swizzled).
-template <int D, int BS>
-__device__ __forceinline__ uint32_t unit_addr(uint32_t base, int r, int ch) {
-  using C = PCfg<D, BS>;
-  return base + (r / C::ROWS) * C::BOX_BYTES + (ch >> 3) * C::ROWS * 128 +
-         (r % C::ROWS) * 128 + (((ch & 7) ^ (r & 7)) << 4);
+// Byte offset of bf16 element (r, c) of a [rows][64] half-tile with the
+// 128-byte swizzle (8-row atoms of 1024 bytes; 16-byte chunks XOR row % 8).
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
 }
 
 template <int D, int BS>
-__global__ void __launch_bounds__(kPThreads)
-prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-               const PrefillArgs a) {
-  using C = PCfg<D, BS>;
-  constexpr int KS = D / 16;  // k-steps of Q K^T
-  constexpr int DT = D / 8;   // n-tiles of the output
+__global__ void __launch_bounds__(kTThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  using C = TCfg<D, BS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  int* smask = reinterpret_cast<int*>(smem + C::MASK_OFF);
+  // bit j of smask[st]: token j of the tile in stage st is present (inside the
+  // sequence and in a valid block)
+  uint64_t* smask = reinterpret_cast<uint64_t*>(smem + C::MASK_OFF);
   volatile int* fault = reinterpret_cast<int*>(smem + C::FAULT_OFF);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;
+  const volatile uint32_t* tmem_slot =
+      reinterpret_cast<const volatile uint32_t*>(smem + C::TMEM_OFF);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int wg = tid >> 7, lr = tid & 127;  // warpgroup; row within it = TMEM lane
+  const uint32_t full0 = sbase + C::BAR_OFF, mma_bar = sbase + C::BAR_OFF + 8 * kTStages;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -99,8 +125,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   const int c = __ldg(&a.cu_q[s + 1]) - cq0;
   const int G = a.group, TQ = a.tile_tokens;
   const int t0 = qt * TQ;
-  // a chunk longer than max_q_len: the rows beyond the grid stay unwritten
-  if (blockIdx.x == 0 && g == 0 && tid == 0 && c > a.n_tiles * TQ)
+  // a chunk longer than max_q_len breaks the contract: flagged (rows beyond
+  // the grid's n_tiles * TQ stay unwritten)
+  if (blockIdx.x == 0 && g == 0 && tid == 0 && c > a.max_q_len)
     report(a.err, PA_DEV_ERR_SEQ_LEN);
   if (c <= 0 || t0 >= c) return;
   int L = __ldg(&a.seq_lens[s]);
@@ -111,250 +138,303 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   }
   const int nt = min(TQ, c - t0);  // query tokens in this tile
 
-  // ---- this thread's two rows (gq and gq + 8 of the warp's 16)
-  int pos[2];
-  int64_t orow[2];
+  // ---- this thread's row of the tile: token t = tid / G, head n = tid % G
+  const int rt = tid / G, rn = tid - rt * G;
+  const bool row_ok = tid < TQ * G && rt < nt && L >= c;
+  const int pos = row_ok ? L - c + t0 + rt : -1;  // -1: no key visible, row not written
+  const int64_t orow = row_ok ? ((int64_t)(cq0 + t0 + rt) * a.n_q + (int64_t)g * G + rn) : -1;
+
+  // ---- Q tile into shared memory (K-major, swizzled); absent rows are zero
+  {
+    const uint4* qr = reinterpret_cast<const uint4*>(a.q + (orow < 0 ? 0 : orow) * D);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = warp * 16 + gq + 8 * h;
-    const int t = r / G, n = r - (r / G) * G;
-    const bool ok = r < TQ * G && t < nt && L >= c;
-    pos[h] = ok ? L - c + t0 + t : -1;  // -1: no key is visible, the row is not written
-    orow[h] = ok ? ((int64_t)(cq0 + t0 + t) * a.n_q + (int64_t)g * G + n) : -1;
-  }
-  // ---- Q fragments (A operand, rows x head_dim)
-  uint32_t qa[KS][4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t* qr = reinterpret_cast<const uint32_t*>(a.q + (orow[h] < 0 ? 0 : orow[h]) * D);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][h] = orow[h] < 0 ? 0u : __ldg(&qr[ks * 8 + cq]);
-      qa[ks][2 + h] = orow[h] < 0 ? 0u : __ldg(&qr[ks * 8 + 4 + cq]);
+    for (int ch = 0; ch < D / 8; ++ch) {
+      const uint4 v = orow < 0 ? make_uint4(0, 0, 0, 0) : __ldg(&qr[ch]);
+      *reinterpret_cast<uint4*>(smem + C::Q_OFF + wg * C::QWG + (ch >> 3) * C::QHALF +
+                                swz128(lr, (ch & 7) * 8)) = v;
     }
   }
-
   const int pmax = L - c + t0 + nt - 1;  // the tile's last position
-  const int n_units = pmax < 0 ? 0 : pmax / kPUnit + 1;
+  const int n_kv = pmax < 0 ? 0 : pmax / kTKv + 1;
   const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
 
+  if (warp == 0) tc_alloc(sbase + C::TMEM_OFF, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < kPStages; ++i) mbar_init(sbase + C::BAR_OFF + 8 * i, 1);
+    for (int i = 0; i <= kTStages; ++i) mbar_init(full0 + 8 * i, 1);
     *fault = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  fence_proxy_async_smem();  // Q (generic writes) before the MMAs read it
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem + wg * 64, tO = tmem + kTmemO + wg * 128;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-  // Unit u's pool blocks (one per box), raw; checked where they are used.
-  auto unit_ids = [&](int u, int (&ids)[C::BOXES]) {
-#pragma unroll
-    for (int b = 0; b < C::BOXES; ++b) {
-      const int tok = u * kPUnit + b * C::ROWS;
-      ids[b] = tok < L ? __ldg(&table[tok / BS]) : -1;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    const uint64_t limit = *fault ? kTWaitAfterFaultNs : kTWaitNs;
+    if (!mbar_wait_bounded(bar, parity, limit)) {
+      report(a.err, PA_DEV_ERR_TIMEOUT);
+      *fault = 1;
     }
   };
-  // Thread 0: load unit u into stage st (absent or invalid boxes skipped).
-  auto issue = [&](int u, int st, const int (&ids)[C::BOXES]) {
-    const uint32_t fb = sbase + C::BAR_OFF + 8 * st;
-    int mask = 0, nload = 0;
+  // Tile kt's pool blocks, one per TMA box, raw (checked where used).
+  constexpr int NB = kTUnits * C::BOXES;
+  int ids_pre[NB];
+  auto tile_ids = [&](int kt, int (&ids)[NB]) {
 #pragma unroll
-    for (int b = 0; b < C::BOXES; ++b) {
-      const int tok = u * kPUnit + b * C::ROWS;
+    for (int i = 0; i < NB; ++i) {
+      const int tok = kt * kTKv + i * C::ROWS;
+      ids[i] = tok < L ? __ldg(&table[tok / BS]) : -1;
+    }
+  };
+  // Thread 0: load K/V tile kt into stage st; absent or invalid boxes skipped.
+  auto issue = [&](int kt, int st, const int (&ids)[NB]) {
+    const uint32_t fb = full0 + 8 * st;
+    uint32_t bytes = 0;
+    uint64_t mask = 0;
+    const int nvalid = min(kTKv, L - kt * kTKv);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int tok = kt * kTKv + i * C::ROWS;
       if (tok >= L) continue;
-      if (ids[b] >= 0 && ids[b] < a.num_blocks) {
-        mask |= 1 << b;
-        ++nload;
+      if (ids[i] >= 0 && ids[i] < a.num_blocks) {
+        mask |= (C::ROWS == 64 ? ~0ull : ((1ull << C::ROWS) - 1)) << (i * C::ROWS);
+        bytes += 2 * C::KH * C::ROWS * 128;
       } else {
         report(a.err, PA_DEV_ERR_BLOCK_ID);
       }
     }
+    if (nvalid < kTKv) mask &= (1ull << nvalid) - 1;
     smask[st] = mask;
-    if (nload == 0) {
+    if (bytes == 0) {
       mbar_arrive(fb);
       return;
     }
-    mbar_arrive_expect_tx(fb, (uint32_t)nload * 2 * C::BOX_BYTES);
-    const uint32_t kdst = sbase + st * C::STAGE, vdst = kdst + C::KV_BYTES;
+    mbar_arrive_expect_tx(fb, bytes);
+    const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE, vdst = kdst + C::KV_BYTES;
 #pragma unroll
-    for (int b = 0; b < C::BOXES; ++b) {
-      if (!(mask >> b & 1)) continue;
-      const int tok_in_block = (u * kPUnit) % BS + b * C::ROWS;
-      const int32_t y = (ids[b] * a.n_kv + g) * BS + (BS > kPUnit ? tok_in_block : 0);
-      if (C::KH == 2 && a.map3d) {
-        tma_load_3d(kdst + b * C::BOX_BYTES, &tmk, 0, y, 0, fb);
-        tma_load_3d(vdst + b * C::BOX_BYTES, &tmv, 0, y, 0, fb);
-      } else {
+    for (int i = 0; i < NB; ++i) {
+      const int tok = kt * kTKv + i * C::ROWS;
+      if (tok >= L || ids[i] < 0 || ids[i] >= a.num_blocks) continue;
+      const int32_t y = (ids[i] * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
 #pragma unroll
-        for (int h = 0; h < C::KH; ++h) {
-          tma_load_2d(kdst + b * C::BOX_BYTES + h * C::ROWS * 128, &tmk, h * 64, y, fb);
-          tma_load_2d(vdst + b * C::BOX_BYTES + h * C::ROWS * 128, &tmv, h * 64, y, fb);
-        }
+      for (int h = 0; h < C::KH; ++h) {
+        const uint32_t off = h * C::HALF + i * C::ROWS * 128;
+        tma_load_2d(kdst + off, &tmk, h * 64, y, fb);
+        tma_load_2d(vdst + off, &tmv, h * 64, y, fb);
       }
     }
   };
-
-  int ids_next[C::BOXES];
-  if (tid == 0) {
-    for (int u = 0; u < n_units && u < kPStages; ++u) {
-      int ids[C::BOXES];
-      unit_ids(u, ids);
-      issue(u, u, ids);
+  // All threads: zero the V rows of tile kt (stage st) that hold no token of
+  // the sequence, so a zero weight times them stays zero; then make the
+  // writes visible to the tensor cores.
+  auto zero_absent = [&](int kt, int st) {
+    const uint64_t mask = smask[st];
+    if (mask == ~0ull) return;
+    uint8_t* vb = smem + C::KV_OFF + st * C::STAGE + C::KV_BYTES;
+    for (int i = tid; i < kTKv * C::KH * 8; i += kTThreads) {
+      const int r = i / (C::KH * 8), rest = i % (C::KH * 8), h = rest / 8, ch = rest % 8;
+      if (!(mask >> r & 1))
+        *reinterpret_cast<uint4*>(vb + h * C::HALF + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
     }
+    fence_proxy_async_smem();
+  };
+  constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
+  constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
+  auto issue_s = [&](int st) {  // S_w = Q_w K^T for both warpgroups
+    const uint32_t kb = sbase + C::KV_OFF + st * C::STAGE;
+#pragma unroll
+    for (int w = 0; w < kTWarpgroups; ++w)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t ad = tc_desc_sw128(
+            sbase + C::Q_OFF + w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32, 16, 1024);
+        const uint64_t bd = tc_desc_sw128(kb + (ks >> 2) * C::HALF + (ks & 3) * 32, 16, 1024);
+        tc_mma_bf16(tmem + w * 64, ad, bd, kIdS, ks > 0);
+      }
+  };
+  auto issue_pv = [&](int st, bool first) {  // O_w += P_hi,w V + P_lo,w V
+    const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE + C::KV_BYTES;
+#pragma unroll
+    for (int w = 0; w < kTWarpgroups; ++w)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < kTKv / 16; ++ks) {
+          const uint64_t ad = tc_desc_sw128(
+              sbase + C::P_OFF + w * C::PWG + part * C::PBUF + ks * 32, 16, 1024);
+          const uint64_t bd = tc_desc_sw128(vb + ks * 2048, C::HALF, 1024);
+          tc_mma_bf16(tmem + kTmemO + w * 128, ad, bd, kIdPV,
+                      !(first && part == 0 && ks == 0));
+        }
+  };
+
+  // ---- prologue: the first stages, S of tile 0
+  if (tid == 0) {
+    int ids[NB];
+    for (int kt = 0; kt < n_kv && kt < kTStages; ++kt) {
+      tile_ids(kt, ids);
+      issue(kt, kt, ids);
+    }
+    if (kTStages < n_kv) tile_ids(kTStages, ids_pre);
+  }
+  if (n_kv > 0) {
+    wait(full0, 0);
+    zero_absent(0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && n_kv > 0) {
+    issue_s(0);
+    tc_commit(mma_bar);
   }
 
-  float acc[DT][4];
-#pragma unroll
-  for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
-  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
-
-  // ldmatrix lane roles: matrix mi = lane / 8, its row lane % 8
-  const int mi = lane >> 3;
-  const int k_row = (lane & 7) + 8 * (mi >> 1), k_ch = mi & 1;  // K: x4 = 2 token groups x 2 chunks
-  const int v_row = (lane & 7) + 8 * (mi & 1), v_ch = mi >> 1;  // V^T: x4 = 2 chunks x 2 token groups
-
+  float m = -INFINITY, l = 0.f;
 #pragma unroll 1
-  for (int u = 0; u < n_units; ++u) {
-    const int st = u % kPStages;
-    if (tid == 0 && u + kPStages < n_units) unit_ids(u + kPStages, ids_next);
-    {
-      const uint64_t limit = *fault ? kPWaitAfterFaultNs : kPWaitNs;
-      if (!mbar_wait_bounded(sbase + C::BAR_OFF + 8 * st, (u / kPStages) & 1, limit)) {
-        report(a.err, PA_DEV_ERR_TIMEOUT);
-        *fault = 1;
+  for (int kt = 0; kt < n_kv; ++kt) {
+    const int st = kt % kTStages;
+    wait(mma_bar, kt & 1);  // S(kt) is in TMEM and P V(kt-1) is done
+    tc_fence_after();
+    if (tid == 0 && kt >= 1 && kt - 1 + kTStages < n_kv) {
+      // stage (kt-1) % S is free: its P V has completed
+      issue(kt - 1 + kTStages, (kt - 1) % kTStages, ids_pre);
+      if (kt + kTStages < n_kv) tile_ids(kt + kTStages, ids_pre);
+    }
+    // ---- this thread's row of S: mask, lazy online softmax. Scores stay in
+    // raw units (the scale, > 0, goes into one FFMA per weight); masked
+    // positions become -inf. On tiles the row sees whole, nothing is masked.
+    uint32_t sr[2][32];
+    tc_ld32(tS + lane_off, sr[0]);
+    tc_ld32(tS + lane_off + 32, sr[1]);
+    tc_wait_ld();
+    const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
+    const uint64_t vis = lim < 0 ? 0ull
+                                 : smask[st] & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+    if (vis == ~0ull) {
+#pragma unroll
+      for (int j = 0; j < kTKv; ++j)
+        mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < kTKv; ++j) {
+        const float x = (vis >> j & 1) ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
+        sr[j >> 5][j & 31] = __float_as_uint(x);
+        mx4[j & 3] = fmaxf(mx4[j & 3], x);
       }
     }
-    const int mask = smask[st];
-    const int j0 = u * kPUnit;
-    const int nvalid = min(kPUnit, L - j0);
-    const uint32_t kb = sbase + st * C::STAGE, vb = kb + C::KV_BYTES;
-    bool all_ok = nvalid == kPUnit;
-#pragma unroll
-    for (int b = 0; b < C::BOXES; ++b)
-      if (b * C::ROWS < nvalid && !(mask >> b & 1)) all_ok = false;
-    if (!all_ok) {
-      // rows of absent tokens may hold anything (even NaN): zero their V so a
-      // zero weight times the row stays zero
-      for (int i = tid; i < kPUnit * C::KH * 8; i += kPThreads) {
-        const int r = i / (C::KH * 8), ch = i % (C::KH * 8);
-        if (r >= nvalid || !(mask >> (r / C::ROWS) & 1))
-          *reinterpret_cast<uint4*>(smem + (unit_addr<D, BS>(vb, r, ch) - sbase)) =
-              make_uint4(0, 0, 0, 0);
-      }
-      fence_proxy_async_smem();  // before the stage is refilled by TMA
-      __syncthreads();
-    }
-
-    // ---- S = Q K^T, 16 rows x 16 tokens per warp
-    float sc[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(unit_addr<D, BS>(kb, k_row, 2 * ks + k_ch), b0, b1, b2, b3);
-      mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-      mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-    }
-    // ---- causal / length / block masks, online softmax (lazy reference)
-    float x[2][4];
-    float rmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int jl = i * 8 + 2 * cq + (e & 1);  // token within the unit
-        const int h = e >> 1;                     // row gq or gq + 8
-        const bool ok = jl < nvalid && (mask >> (jl / C::ROWS) & 1) && j0 + jl <= pos[h];
-        x[i][e] = ok ? sc[i][e] * a.scale_log2 : -INFINITY;
-        rmax[h] = fmaxf(rmax[h], x[i][e]);
-      }
-    const bool need = rmax[0] > mrun[0] + kPLazyLog2 || rmax[1] > mrun[1] + kPLazyLog2;
+    const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
+    const bool need = rmax > m + kTLazyLog2;
     if (__any_sync(0xffffffffu, need)) {
+      const float m_new = need ? fmaxf(m, rmax) : m;
+      const float alpha = fast_exp2(m - (m_new == -INFINITY ? 0.f : m_new));
+      if (kt > 0) {  // O holds earlier tiles: rescale this warp's rows
+        const float f = need ? alpha : 1.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = rmax[h];
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(mrun[h], mx);
-        const float alpha = fast_exp2(mrun[h] - (m_new == -INFINITY ? 0.f : m_new));
-        lrun[h] *= alpha;
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tc_ld32(tO + lane_off + cc, o);
+          tc_wait_ld();
 #pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          acc[dt][2 * h] *= alpha;
-          acc[dt][2 * h + 1] *= alpha;
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tc_st32(tO + lane_off + cc, o);
         }
-        mrun[h] = m_new;
+        tc_wait_st();
+      }
+      if (need) {
+        l *= alpha;
+        m = m_new;
       }
     }
-    float p[2][4];
+    const float nbase = m == -INFINITY ? 0.f : -m;
+    const float sl2 = a.scale_log2;
+    // P as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): a lone bf16
+    // weight is off by up to 2^-9 relative, which on rows that see only a few
+    // keys (the start of a prompt) is as large as the whole output tolerance.
+    uint8_t* ph = smem + C::P_OFF + wg * C::PWG;
+    uint8_t* pl = ph + C::PBUF;
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = e >> 1;
-        p[i][e] = fast_exp2(x[i][e] - (mrun[h] == -INFINITY ? 0.f : mrun[h]));
-        lrun[h] += p[i][e];
+      for (int k = 0; k < 4; ++k) {
+        const int j = ch * 8 + 2 * k;
+        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j >> 5][j & 31]), sl2, nbase));
+        const float p1 =
+            fast_exp2(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), sl2, nbase));
+        l4[k] += p0 + p1;
+        hw[k] = pack_bf16x2(p0, p1);
+        lw[k] = pack_bf16x2(p0 - __uint_as_float(hw[k] << 16),
+                            p1 - __uint_as_float(hw[k] & 0xffff0000u));
       }
-    // P as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): a lone
-    // bf16 weight is off by up to 2^-9 relative, which on rows that see only
-    // a few keys (the start of a prompt) is as large as the whole output
-    // tolerance; the pair is good to about 2^-17.
-    uint32_t ph[4], pl[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo_in = p[k >> 1][(k & 1) * 2], hi_in = p[k >> 1][(k & 1) * 2 + 1];
-      ph[k] = pack_bf16x2(lo_in, hi_in);
-      pl[k] = pack_bf16x2(lo_in - __uint_as_float(ph[k] << 16),
-                          hi_in - __uint_as_float(ph[k] & 0xffff0000u));
+      const uint32_t off = lr * 128 + (((ch ^ lr) & 7) << 4);
+      *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    // ---- O += P V
-#pragma unroll
-    for (int dp = 0; dp < DT / 2; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_trans(unit_addr<D, BS>(vb, v_row, 2 * dp + v_ch), b0, b1, b2, b3);
-      mma_bf16_16816(acc[2 * dp], ph[0], ph[1], ph[2], ph[3], b0, b1);
-      mma_bf16_16816(acc[2 * dp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-      mma_bf16_16816(acc[2 * dp], pl[0], pl[1], pl[2], pl[3], b0, b1);
-      mma_bf16_16816(acc[2 * dp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+    l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+    fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
+    // the next tile's K/V must be in shared memory before its S is issued
+    if (kt + 1 < n_kv) {
+      wait(full0 + 8 * ((kt + 1) % kTStages), ((kt + 1) / kTStages) & 1);
+      zero_absent(kt + 1, (kt + 1) % kTStages);
     }
-    __syncthreads();  // every warp is done with stage st
-    if (tid == 0 && u + kPStages < n_units) issue(u + kPStages, st, ids_next);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      issue_pv(st, kt == 0);
+      if (kt + 1 < n_kv) issue_s((kt + 1) % kTStages);
+      tc_commit(mma_bar);
+    }
   }
 
   // ---- normalise and write the rows
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float l = lrun[h];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (orow[h] < 0) continue;
+  if (n_kv > 0) {
+    wait(mma_bar, n_kv & 1);  // the last P V
+    tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(a.out + orow[h] * D);
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt)
-      o[dt * 4 + cq] = __floats2bfloat162_rn(acc[dt][2 * h] * inv, acc[dt][2 * h + 1] * inv);
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t o[32];
+      tc_ld32(tO + lane_off + cc, o);
+      tc_wait_ld();
+      if (orow >= 0) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            w[k] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * k]) * inv,
+                               __uint_as_float(o[v * 8 + 2 * k + 1]) * inv);
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc_dealloc(tmem, kTmemCols);
 }
 
 template <int D, int BS>
 pa_status launch_prefill(PrefillArgs a, const void* k_pool, const void* v_pool,
                          cudaStream_t stream) {
-  using C = PCfg<D, BS>;
+  using C = TCfg<D, BS>;
   const int64_t rows = (int64_t)a.num_blocks * a.n_kv * BS;
   CUtensorMap tmk, tmv;
-  int k3 = 0, v3 = 0;
-  pa_status st = make_pool_map(&tmk, k_pool, D, 2, rows, C::ROWS, true, &k3);
+  int k3 = 0, v3 = 0;  // 2-D maps: each 64-column half lands in its own slab
+  pa_status st = make_pool_map(&tmk, k_pool, D, 2, rows, C::ROWS, false, &k3);
   if (st != PA_OK) return st;
-  st = make_pool_map(&tmv, v_pool, D, 2, rows, C::ROWS, k3 == 1, &v3);
+  st = make_pool_map(&tmv, v_pool, D, 2, rows, C::ROWS, false, &v3);
   if (st != PA_OK) return st;
-  if (k3 != v3) {
-    st = make_pool_map(&tmk, k_pool, D, 2, rows, C::ROWS, false, &k3);
-    if (st != PA_OK) return st;
-  }
-  a.map3d = k3 && v3;
-  auto kern = prefill_kernel<D, BS>;
+  auto kern = prefill_tc_kernel<D, BS>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
@@ -367,7 +447,7 @@ pa_status launch_prefill(PrefillArgs a, const void* k_pool, const void* v_pool,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_tiles, (unsigned)a.num_seqs, (unsigned)a.n_kv);
-  cfg.blockDim = dim3(kPThreads);
+  cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -403,10 +483,11 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   if (n_q_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
   const int G = n_q_heads / n_kv_heads;
   if ((head_dim != 64 && head_dim != 128) ||
-      (block_size != 8 && block_size != 16 && block_size != 32) || G > kPRows)
+      (block_size != 8 && block_size != 16 && block_size != 32) || G > 64)
     return PA_ERR_UNSUPPORTED;
   if ((int64_t)num_blocks * n_kv_heads * block_size >= (int64_t)1 << 31)
     return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale == INFINITY) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || max_q_len == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !cu_q)
     return PA_ERR_INVALID_ARG;
@@ -425,12 +506,12 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   a.n_q = n_q_heads;
   a.n_kv = n_kv_heads;
   a.group = G;
-  a.tile_tokens = kPRows / G;
+  a.tile_tokens = kTTileRows / G;
   const int64_t tiles = ((int64_t)max_q_len + a.tile_tokens - 1) / a.tile_tokens;
   if (tiles > 2147483647) return PA_ERR_INVALID_ARG;
   a.n_tiles = (int)tiles;
-  a.map3d = 0;
-  a.scale_log2 = scale * kPLog2e;
+  a.max_q_len = max_q_len;
+  a.scale_log2 = scale * kTLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 64) return prefill_bs<64>(block_size, a, k_pool, v_pool, st);
   return prefill_bs<128>(block_size, a, k_pool, v_pool, st);

@@ -49,7 +49,7 @@ CASES = [
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32])
-@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (12, 4), (16, 1)])
+@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (12, 4), (16, 1), (64, 2)])
 def test_prefill_parity(d, bs, heads):
     Hq, Hkv = heads
     for i, (ctx, ch) in enumerate(CASES):
