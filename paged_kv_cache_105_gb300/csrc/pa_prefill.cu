@@ -24,8 +24,9 @@
 //    (rescaling its row of O in TMEM in the rare case the reference moves),
 //    and writes P to shared memory as a bf16 pair hi + lo; then
 //    O += P_hi V + P_lo V (M 128, N head_dim, V read MN-major) accumulates in
-//    TMEM. One thread issues the MMAs; one mbarrier commit per tile covers
-//    the P V of this tile and the S of the next.
+//    TMEM. One thread issues the MMAs. S is double-buffered in TMEM: S of the
+//    next tile and P V of the previous one run on the tensor cores while the
+//    threads compute the softmax of the current one.
 //  * O is normalised and written as bf16 after the last tile.
 // Tiles are numbered so a sequence's latest (longest) tiles start first.
 #include <cuda.h>
@@ -41,16 +42,22 @@ namespace pa {
 namespace {
 
 constexpr int kTWarpgroups = 2;             // each owns 128 rows (one MMA M)
-constexpr int kTThreads = 128 * kTWarpgroups;
+constexpr int kTThreads = 128 * kTWarpgroups;  // softmax threads, one per row
+constexpr int kTMmaWarp = kTThreads / 32;       // then one warp issuing the MMAs
+constexpr int kTLoadWarp = kTMmaWarp + 1;       // and one warp issuing the copies
+constexpr int kTCtaThreads = kTThreads + 64;
 constexpr int kTRows = 128;                 // M of every MMA: rows per warpgroup
 constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
 constexpr int kTKv = 64;                    // K/V tokens per tile (N of S)
 constexpr int kTUnit = 16;                  // tokens per TMA unit
-constexpr int kTUnits = kTKv / kTUnit;
 constexpr int kTStages = 3;
-// TMEM columns: S of warpgroup w at 64 w, its O at 128 + 128 w
+// TMEM columns: S of warpgroup w in buffer 0 at 64 w and in buffer 1 at
+// 384 + 64 w; its O at 128 + 128 w
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;
+__host__ __device__ constexpr uint32_t tmem_s_col(int w, int b) {
+  return b ? 384 + 64 * w : 64 * w;
+}
 constexpr uint64_t kTWaitNs = 2000000000ull;      // 2 s: a wait that long is a fault
 constexpr uint64_t kTWaitAfterFaultNs = 1000000ull;
 constexpr float kTLazyLog2 = 8.f;
@@ -73,21 +80,25 @@ struct PrefillArgs {
 template <int D, int BS>
 struct TCfg {
   static constexpr int ROWS = BS < kTUnit ? BS : kTUnit;  // rows per TMA box
-  static constexpr int BOXES = kTUnit / ROWS;             // boxes per unit
+  static constexpr int NB = kTKv / ROWS;                  // boxes (blocks) per tile
   static constexpr int KH = D / 64;                       // 64-column halves
   static constexpr int HALF = kTKv * 128;                 // one half of K (or V): 8 KB
   static constexpr int KV_BYTES = KH * HALF;
-  static constexpr int STAGE = 2 * KV_BYTES;
   static constexpr int QHALF = kTRows * 128;              // 16 KB
   static constexpr int QWG = KH * QHALF;                  // one warpgroup's Q
   static constexpr int Q_OFF = 0;
   static constexpr int PBUF = kTRows * 128;
   static constexpr int PWG = 2 * PBUF;                    // P hi, then P lo
   static constexpr int P_OFF = Q_OFF + kTWarpgroups * QWG;
-  static constexpr int KV_OFF = P_OFF + kTWarpgroups * PWG;
-  static constexpr int BAR_OFF = KV_OFF + kTStages * STAGE;  // full[3], mma
-  static constexpr int MASK_OFF = BAR_OFF + (kTStages + 1) * 8;  // 64-bit token masks
-  static constexpr int TMEM_OFF = MASK_OFF + kTStages * 8;
+  // K stages [kTStages][KV_BYTES], then V stages: K of a tile is freed by its
+  // S, well before its V is freed by its P V, so each streams on its own ring
+  static constexpr int K_OFF = P_OFF + kTWarpgroups * PWG;
+  static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
+  // fullK[3], fullV[3], emptyK[3], emptyV[3], S done (one per S buffer),
+  // P V done, P written
+  static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
+  static constexpr int NBARS = 4 * kTStages + 4;
+  static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
   static constexpr size_t SMEM = 1024 + FAULT_OFF + 8;
 };
@@ -98,24 +109,33 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
 }
 
+// Three roles: eight softmax warps (one row per thread), one warp whose lane
+// 0 issues the MMAs, one warp whose lane 0 issues the TMA copies. They meet
+// only at mbarriers, each of which a waiter can never fall two phases behind:
+//   fullK/fullV[st]  copies landed          (loader -> MMA issuer)
+//   emptyK/emptyV[st] S / P V of the tile done (MMA commit -> loader)
+//   s_bar[b]         S of the tile in buffer b (MMA commit -> softmax)
+//   pv_bar           P V of the tile done     (MMA commit -> softmax)
+//   p_bar            P of the tile written    (256 softmax arrivals -> MMA issuer)
 template <int D, int BS>
-__global__ void __launch_bounds__(kTThreads, 1)
+__global__ void __launch_bounds__(kTCtaThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
   using C = TCfg<D, BS>;
+  constexpr int NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  // bit j of smask[st]: token j of the tile in stage st is present (inside the
-  // sequence and in a valid block)
-  uint64_t* smask = reinterpret_cast<uint64_t*>(smem + C::MASK_OFF);
   volatile int* fault = reinterpret_cast<int*>(smem + C::FAULT_OFF);
   const volatile uint32_t* tmem_slot =
       reinterpret_cast<const volatile uint32_t*>(smem + C::TMEM_OFF);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int wg = tid >> 7, lr = tid & 127;  // warpgroup; row within it = TMEM lane
-  const uint32_t full0 = sbase + C::BAR_OFF, mma_bar = sbase + C::BAR_OFF + 8 * kTStages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool softmax = warp < kTMmaWarp;
+  const int wg = (tid >> 7) & 1, lr = tid & 127;  // warpgroup; row within it = TMEM lane
+  const uint32_t fullK = sbase + C::BAR_OFF, fullV = fullK + 8 * kTStages;
+  const uint32_t emptyK = fullV + 8 * kTStages, emptyV = emptyK + 8 * kTStages;
+  const uint32_t s_bar = emptyV + 8 * kTStages, pv_bar = s_bar + 16, p_bar = pv_bar + 8;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -140,12 +160,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 
   // ---- this thread's row of the tile: token t = tid / G, head n = tid % G
   const int rt = tid / G, rn = tid - rt * G;
-  const bool row_ok = tid < TQ * G && rt < nt && L >= c;
+  const bool row_ok = softmax && tid < TQ * G && rt < nt && L >= c;
   const int pos = row_ok ? L - c + t0 + rt : -1;  // -1: no key visible, row not written
   const int64_t orow = row_ok ? ((int64_t)(cq0 + t0 + rt) * a.n_q + (int64_t)g * G + rn) : -1;
 
   // ---- Q tile into shared memory (K-major, swizzled); absent rows are zero
-  {
+  if (softmax) {
     const uint4* qr = reinterpret_cast<const uint4*>(a.q + (orow < 0 ? 0 : orow) * D);
 #pragma unroll
     for (int ch = 0; ch < D / 8; ++ch) {
@@ -160,19 +180,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 
   if (warp == 0) tc_alloc(sbase + C::TMEM_OFF, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i <= kTStages; ++i) mbar_init(full0 + 8 * i, 1);
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(fullK + 8 * i, 1);
+    mbar_init(p_bar, kTThreads);  // every softmax thread arrives once per tile
     *fault = 0;
     fence_mbarrier_init();
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
   }
   fence_proxy_async_smem();  // Q (generic writes) before the MMAs read it
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem + wg * 64, tO = tmem + kTmemO + wg * 128;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
   auto wait = [&](uint32_t bar, uint32_t parity) {
     const uint64_t limit = *fault ? kTWaitAfterFaultNs : kTWaitNs;
@@ -181,9 +198,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       *fault = 1;
     }
   };
-  // Tile kt's pool blocks, one per TMA box, raw (checked where used).
-  constexpr int NB = kTUnits * C::BOXES;
-  int ids_pre[NB];
+  // Tile kt's pool blocks, one per TMA box, raw (checked where used), and the
+  // mask of its tokens present in the pool (inside the sequence, valid block).
   auto tile_ids = [&](int kt, int (&ids)[NB]) {
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
@@ -191,229 +207,244 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       ids[i] = tok < L ? __ldg(&table[tok / BS]) : -1;
     }
   };
-  // Thread 0: load K/V tile kt into stage st; absent or invalid boxes skipped.
-  auto issue = [&](int kt, int st, const int (&ids)[NB]) {
-    const uint32_t fb = full0 + 8 * st;
-    uint32_t bytes = 0;
+  auto tile_mask = [&](int kt, const int (&ids)[NB]) {
     uint64_t mask = 0;
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+      if (ids[i] >= 0 && ids[i] < a.num_blocks)
+        mask |= ((1ull << C::ROWS) - 1) << (i * C::ROWS);
     const int nvalid = min(kTKv, L - kt * kTKv);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      const int tok = kt * kTKv + i * C::ROWS;
-      if (tok >= L) continue;
-      if (ids[i] >= 0 && ids[i] < a.num_blocks) {
-        mask |= (C::ROWS == 64 ? ~0ull : ((1ull << C::ROWS) - 1)) << (i * C::ROWS);
-        bytes += 2 * C::KH * C::ROWS * 128;
-      } else {
-        report(a.err, PA_DEV_ERR_BLOCK_ID);
-      }
-    }
     if (nvalid < kTKv) mask &= (1ull << nvalid) - 1;
-    smask[st] = mask;
-    if (bytes == 0) {
-      mbar_arrive(fb);
-      return;
-    }
-    mbar_arrive_expect_tx(fb, bytes);
-    const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE, vdst = kdst + C::KV_BYTES;
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      const int tok = kt * kTKv + i * C::ROWS;
-      if (tok >= L || ids[i] < 0 || ids[i] >= a.num_blocks) continue;
-      const int32_t y = (ids[i] * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
-#pragma unroll
-      for (int h = 0; h < C::KH; ++h) {
-        const uint32_t off = h * C::HALF + i * C::ROWS * 128;
-        tma_load_2d(kdst + off, &tmk, h * 64, y, fb);
-        tma_load_2d(vdst + off, &tmv, h * 64, y, fb);
-      }
-    }
-  };
-  // All threads: zero the V rows of tile kt (stage st) that hold no token of
-  // the sequence, so a zero weight times them stays zero; then make the
-  // writes visible to the tensor cores.
-  auto zero_absent = [&](int kt, int st) {
-    const uint64_t mask = smask[st];
-    if (mask == ~0ull) return;
-    uint8_t* vb = smem + C::KV_OFF + st * C::STAGE + C::KV_BYTES;
-    for (int i = tid; i < kTKv * C::KH * 8; i += kTThreads) {
-      const int r = i / (C::KH * 8), rest = i % (C::KH * 8), h = rest / 8, ch = rest % 8;
-      if (!(mask >> r & 1))
-        *reinterpret_cast<uint4*>(vb + h * C::HALF + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
-  };
-  constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
-  constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
-  auto issue_s = [&](int st) {  // S_w = Q_w K^T for both warpgroups
-    const uint32_t kb = sbase + C::KV_OFF + st * C::STAGE;
-#pragma unroll
-    for (int w = 0; w < kTWarpgroups; ++w)
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint64_t ad = tc_desc_sw128(
-            sbase + C::Q_OFF + w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = tc_desc_sw128(kb + (ks >> 2) * C::HALF + (ks & 3) * 32, 16, 1024);
-        tc_mma_bf16(tmem + w * 64, ad, bd, kIdS, ks > 0);
-      }
-  };
-  auto issue_pv = [&](int st, bool first) {  // O_w += P_hi,w V + P_lo,w V
-    const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE + C::KV_BYTES;
-#pragma unroll
-    for (int w = 0; w < kTWarpgroups; ++w)
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < kTKv / 16; ++ks) {
-          const uint64_t ad = tc_desc_sw128(
-              sbase + C::P_OFF + w * C::PWG + part * C::PBUF + ks * 32, 16, 1024);
-          const uint64_t bd = tc_desc_sw128(vb + ks * 2048, C::HALF, 1024);
-          tc_mma_bf16(tmem + kTmemO + w * 128, ad, bd, kIdPV,
-                      !(first && part == 0 && ks == 0));
-        }
+    return mask;
   };
 
-  // ---- prologue: the first stages, S of tile 0
-  if (tid == 0) {
-    int ids[NB];
-    for (int kt = 0; kt < n_kv && kt < kTStages; ++kt) {
-      tile_ids(kt, ids);
-      issue(kt, kt, ids);
-    }
-    if (kTStages < n_kv) tile_ids(kTStages, ids_pre);
-  }
-  if (n_kv > 0) {
-    wait(full0, 0);
-    zero_absent(0, 0);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0 && n_kv > 0) {
-    issue_s(0);
-    tc_commit(mma_bar);
-  }
-
-  float m = -INFINITY, l = 0.f;
+  if (warp == kTLoadWarp) {
+    // ---- copies: K and V of every tile through their 3-stage rings
+    if (lane == 0) {
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
 #pragma unroll 1
-  for (int kt = 0; kt < n_kv; ++kt) {
-    const int st = kt % kTStages;
-    wait(mma_bar, kt & 1);  // S(kt) is in TMEM and P V(kt-1) is done
-    tc_fence_after();
-    if (tid == 0 && kt >= 1 && kt - 1 + kTStages < n_kv) {
-      // stage (kt-1) % S is free: its P V has completed
-      issue(kt - 1 + kTStages, (kt - 1) % kTStages, ids_pre);
-      if (kt + kTStages < n_kv) tile_ids(kt + kTStages, ids_pre);
-    }
-    // ---- this thread's row of S: mask, lazy online softmax. Scores stay in
-    // raw units (the scale, > 0, goes into one FFMA per weight); masked
-    // positions become -inf. On tiles the row sees whole, nothing is masked.
-    uint32_t sr[2][32];
-    tc_ld32(tS + lane_off, sr[0]);
-    tc_ld32(tS + lane_off + 32, sr[1]);
-    tc_wait_ld();
-    const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
-    const uint64_t vis = lim < 0 ? 0ull
-                                 : smask[st] & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
-    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
-    if (vis == ~0ull) {
+      for (int kt = 0; kt < n_kv; ++kt) {
+        const int st = kt % kTStages;
+        int ids[NB];
+        tile_ids(kt, ids);
+        uint32_t bytes = 0;
 #pragma unroll
-      for (int j = 0; j < kTKv; ++j)
-        mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
-    } else {
-#pragma unroll
-      for (int j = 0; j < kTKv; ++j) {
-        const float x = (vis >> j & 1) ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
-        sr[j >> 5][j & 31] = __float_as_uint(x);
-        mx4[j & 3] = fmaxf(mx4[j & 3], x);
-      }
-    }
-    const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
-    const bool need = rmax > m + kTLazyLog2;
-    if (__any_sync(0xffffffffu, need)) {
-      const float m_new = need ? fmaxf(m, rmax) : m;
-      const float alpha = fast_exp2(m - (m_new == -INFINITY ? 0.f : m_new));
-      if (kt > 0) {  // O holds earlier tiles: rescale this warp's rows
-        const float f = need ? alpha : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tc_ld32(tO + lane_off + cc, o);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tc_st32(tO + lane_off + cc, o);
+        for (int i = 0; i < NB; ++i) {
+          const int tok = kt * kTKv + i * C::ROWS;
+          if (tok >= L) continue;
+          if (ids[i] >= 0 && ids[i] < a.num_blocks) bytes += C::KH * C::ROWS * 128;
+          else report(a.err, PA_DEV_ERR_BLOCK_ID);
         }
-        tc_wait_st();
+        for (int kv = 0; kv < 2; ++kv) {
+          if (kt >= kTStages)  // the stage's previous tile is done with it
+            wait((kv ? emptyV : emptyK) + 8 * st, ((kt - kTStages) / kTStages) & 1);
+          const uint32_t fb = (kv ? fullV : fullK) + 8 * st;
+          if (bytes == 0) {
+            mbar_arrive(fb);
+            continue;
+          }
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t dst = sbase + (kv ? C::V_OFF : C::K_OFF) + st * C::KV_BYTES;
+#pragma unroll
+          for (int i = 0; i < NB; ++i) {
+            const int tok = kt * kTKv + i * C::ROWS;
+            if (tok >= L || ids[i] < 0 || ids[i] >= a.num_blocks) continue;
+            const int32_t y = (ids[i] * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
+#pragma unroll
+            for (int h = 0; h < C::KH; ++h)
+              tma_load_2d(dst + h * C::HALF + i * C::ROWS * 128, kv ? &tmv : &tmk, h * 64, y,
+                          fb);
+          }
+        }
       }
+    }
+    __syncwarp();
+  } else if (warp == kTMmaWarp) {
+    // ---- MMAs, in tile order: S(kt+1) as soon as K(kt+1) has landed (S is
+    // double-buffered in TMEM, so it runs during the softmax of kt), then
+    // P V(kt) once the softmax threads have written P(kt).
+    if (lane == 0 && n_kv > 0) {
+      // Operand descriptors: built once; the start address sits in the low
+      // 14 bits in 16-byte units (shared addresses stay below 2^18), so an
+      // offset into a tile is added to the descriptor directly.
+      const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
+      const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
+      const uint64_t dp = tc_desc_sw128(sbase + C::P_OFF, 16, 1024);
+      const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
+      constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
+      constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
+      auto issue_s = [&](int kt) {  // S_w = Q_w K^T for both warpgroups
+        const int st = kt % kTStages, buf = kt & 1;
+        wait(fullK + 8 * st, (kt / kTStages) & 1);
+        tc_fence_after();
+        const uint64_t kb = dk + ((st * C::KV_BYTES) >> 4);
+#pragma unroll
+        for (int w = 0; w < kTWarpgroups; ++w)
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = ((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4;
+            const uint32_t qoff = (w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4;
+            tc_mma_bf16(tmem + tmem_s_col(w, buf), dq + qoff, kb + koff, kIdS, ks > 0);
+          }
+        tc_commit(s_bar + 8 * buf);
+        tc_commit(emptyK + 8 * st);
+      };
+      issue_s(0);
+#pragma unroll 1
+      for (int kt = 0; kt < n_kv; ++kt) {
+        const int st = kt % kTStages;
+        // S(kt+1)'s buffer was last read by the softmax of kt-1 (p_bar(kt-1))
+        if (kt + 1 < n_kv) issue_s(kt + 1);
+        wait(p_bar, kt & 1);  // P(kt) written, S(kt) read, P V(kt-1) complete
+        wait(fullV + 8 * st, (kt / kTStages) & 1);
+        tc_fence_after();
+        const uint64_t vb = dv + ((st * C::KV_BYTES) >> 4);
+#pragma unroll
+        for (int w = 0; w < kTWarpgroups; ++w)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < kTKv / 16; ++ks)
+              tc_mma_bf16(tmem + kTmemO + w * 128,
+                          dp + ((w * C::PWG + part * C::PBUF + ks * 32) >> 4), vb + ks * 128,
+                          kIdPV, !(kt == 0 && part == 0 && ks == 0));
+        tc_commit(pv_bar);
+        tc_commit(emptyV + 8 * st);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- the softmax warps: one row per thread
+    const uint32_t tO = tmem + kTmemO + wg * 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    int ids_nxt[NB];
+    if (n_kv > 0) tile_ids(0, ids_nxt);
+#pragma unroll 1
+    for (int kt = 0; kt < n_kv; ++kt) {
+      const int st = kt % kTStages;
+      const uint64_t tmask = tile_mask(kt, ids_nxt);
+      if (kt + 1 < n_kv) tile_ids(kt + 1, ids_nxt);  // in flight during this tile
+      wait(s_bar + 8 * (kt & 1), (kt >> 1) & 1);  // S(kt) is in TMEM
+      tc_fence_after();
+      // masked, lazy online softmax of this thread's row. Scores stay in raw
+      // units (the scale, > 0, goes into one FFMA per weight); masked
+      // positions become -inf. On tiles the row sees whole, nothing is masked.
+      uint32_t sr[2][32];
+      const uint32_t tS = tmem + tmem_s_col(wg, kt & 1);
+      tc_ld32(tS + lane_off, sr[0]);
+      tc_ld32(tS + lane_off + 32, sr[1]);
+      tc_wait_ld();
+      const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
+      const uint64_t vis = lim < 0 ? 0ull : tmask & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+      if (vis == ~0ull) {
+#pragma unroll
+        for (int j = 0; j < kTKv; ++j)
+          mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < kTKv; ++j) {
+          const float x = (vis >> j & 1) ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
+          sr[j >> 5][j & 31] = __float_as_uint(x);
+          mx4[j & 3] = fmaxf(mx4[j & 3], x);
+        }
+      }
+      const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
+      const bool need = rmax > m + kTLazyLog2;
+      const bool warp_need = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
       if (need) {
-        l *= alpha;
+        const float m_new = fmaxf(m, rmax);
+        alpha = fast_exp2(m - (m_new == -INFINITY ? 0.f : m_new));
         m = m_new;
       }
-    }
-    const float nbase = m == -INFINITY ? 0.f : -m;
-    const float sl2 = a.scale_log2;
-    // P as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): a lone bf16
-    // weight is off by up to 2^-9 relative, which on rows that see only a few
-    // keys (the start of a prompt) is as large as the whole output tolerance.
-    uint8_t* ph = smem + C::P_OFF + wg * C::PWG;
-    uint8_t* pl = ph + C::PBUF;
-    float l4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
+      const float nbase = m == -INFINITY ? 0.f : -m;
+      const float sl2 = a.scale_log2;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
+      // P as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): a lone
+      // bf16 weight is off by up to 2^-9 relative, which on rows that see only
+      // a few keys (the start of a prompt) is as large as the whole tolerance.
+      uint32_t pk[2][32];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int j = ch * 8 + 2 * k;
-        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j >> 5][j & 31]), sl2, nbase));
+      for (int k = 0; k < 32; ++k) {
+        const float p0 =
+            fast_exp2(fmaf(__uint_as_float(sr[(2 * k) >> 5][(2 * k) & 31]), sl2, nbase));
         const float p1 =
-            fast_exp2(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), sl2, nbase));
-        l4[k] += p0 + p1;
-        hw[k] = pack_bf16x2(p0, p1);
-        lw[k] = pack_bf16x2(p0 - __uint_as_float(hw[k] << 16),
-                            p1 - __uint_as_float(hw[k] & 0xffff0000u));
+            fast_exp2(fmaf(__uint_as_float(sr[(2 * k + 1) >> 5][(2 * k + 1) & 31]), sl2, nbase));
+        l4[k & 3] += p0 + p1;
+        pk[0][k] = pack_bf16x2(p0, p1);
+        pk[1][k] = pack_bf16x2(p0 - __uint_as_float(pk[0][k] << 16),
+                               p1 - __uint_as_float(pk[0][k] & 0xffff0000u));
       }
-      const uint32_t off = lr * 128 + (((ch ^ lr) & 7) << 4);
-      *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+      // P V(kt-1) must be done before O is rescaled and the P buffers reused
+      if (kt > 0) {
+        wait(pv_bar, (kt - 1) & 1);
+        tc_fence_after();
+        if (warp_need) {  // rescale this warp's rows of O (alpha = 1 for the others)
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tc_ld32(tO + lane_off + cc, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc_st32(tO + lane_off + cc, o);
+          }
+          tc_wait_st();
+        }
+      }
+      uint8_t* ph = smem + C::P_OFF + wg * C::PWG;
+      uint8_t* pl = ph + C::PBUF;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = lr * 128 + (((ch ^ lr) & 7) << 4);
+        *reinterpret_cast<uint4*>(ph + off) =
+            make_uint4(pk[0][4 * ch], pk[0][4 * ch + 1], pk[0][4 * ch + 2], pk[0][4 * ch + 3]);
+        *reinterpret_cast<uint4*>(pl + off) =
+            make_uint4(pk[1][4 * ch], pk[1][4 * ch + 1], pk[1][4 * ch + 2], pk[1][4 * ch + 3]);
+      }
+      if (tmask != ~0ull) {
+        // V rows with no token of the sequence may hold anything (even NaN):
+        // zero them so that a zero weight times them stays zero (rare: the
+        // sequence's last tile or a bad block)
+        wait(fullV + 8 * st, (kt / kTStages) & 1);
+        uint8_t* vb = smem + C::V_OFF + st * C::KV_BYTES;
+        for (int i = tid; i < kTKv * C::KH * 8; i += kTThreads) {
+          const int r = i / (C::KH * 8), rest = i % (C::KH * 8), h = rest / 8, ch = rest % 8;
+          if (!(tmask >> r & 1))
+            *reinterpret_cast<uint4*>(vb + h * C::HALF + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();  // P and zeroed rows before the MMA reads them
+      tc_fence_before();
+      mbar_arrive(p_bar);
     }
-    l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-    fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
-    // the next tile's K/V must be in shared memory before its S is issued
-    if (kt + 1 < n_kv) {
-      wait(full0 + 8 * ((kt + 1) % kTStages), ((kt + 1) / kTStages) & 1);
-      zero_absent(kt + 1, (kt + 1) % kTStages);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      issue_pv(st, kt == 0);
-      if (kt + 1 < n_kv) issue_s((kt + 1) % kTStages);
-      tc_commit(mma_bar);
-    }
-  }
 
-  // ---- normalise and write the rows
-  if (n_kv > 0) {
-    wait(mma_bar, n_kv & 1);  // the last P V
-    tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // ---- normalise and write the rows
+    if (n_kv > 0) {
+      wait(pv_bar, (n_kv - 1) & 1);  // the last P V
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
-      uint32_t o[32];
-      tc_ld32(tO + lane_off + cc, o);
-      tc_wait_ld();
-      if (orow >= 0) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc);
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        tc_ld32(tO + lane_off + cc, o);
+        tc_wait_ld();
+        if (orow >= 0) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t w[4];
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            w[k] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * k]) * inv,
-                               __uint_as_float(o[v * 8 + 2 * k + 1]) * inv);
-          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int k = 0; k < 4; ++k)
+              w[k] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * k]) * inv,
+                                 __uint_as_float(o[v * 8 + 2 * k + 1]) * inv);
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
     }
@@ -447,7 +478,7 @@ pa_status launch_prefill(PrefillArgs a, const void* k_pool, const void* v_pool,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_tiles, (unsigned)a.num_seqs, (unsigned)a.n_kv);
-  cfg.blockDim = dim3(kTThreads);
+  cfg.blockDim = dim3(kTCtaThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cfg.attrs = attr;
