@@ -43,9 +43,12 @@ namespace {
 
 constexpr int kTWarpgroups = 2;             // each owns 128 rows (one MMA M)
 constexpr int kTThreads = 128 * kTWarpgroups;  // softmax threads, one per row
-constexpr int kTMmaWarp = kTThreads / 32;       // then one warp issuing the MMAs
-constexpr int kTLoadWarp = kTMmaWarp + 1;       // and one warp issuing the copies
-constexpr int kTCtaThreads = kTThreads + 64;
+// then three single-lane roles, each on its own warp scheduler: S = Q K^T
+// issue, TMA copies, P V issue
+constexpr int kTSWarp = kTThreads / 32;
+constexpr int kTLoadWarp = kTSWarp + 1;
+constexpr int kTPVWarp = kTSWarp + 2;
+constexpr int kTCtaThreads = kTThreads + 96;
 constexpr int kTRows = 128;                 // M of every MMA: rows per warpgroup
 constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
 constexpr int kTKv = 64;                    // K/V tokens per tile (N of S)
@@ -95,9 +98,9 @@ struct TCfg {
   static constexpr int K_OFF = P_OFF + kTWarpgroups * PWG;
   static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
   // fullK[3], fullV[3], emptyK[3], emptyV[3], S done (one per S buffer),
-  // P V done, P written
+  // P V done, P written, S read (one per S buffer)
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
-  static constexpr int NBARS = 4 * kTStages + 4;
+  static constexpr int NBARS = 4 * kTStages + 6;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
   static constexpr size_t SMEM = 1024 + FAULT_OFF + 8;
@@ -109,14 +112,17 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
 }
 
-// Three roles: eight softmax warps (one row per thread), one warp whose lane
-// 0 issues the MMAs, one warp whose lane 0 issues the TMA copies. They meet
-// only at mbarriers, each of which a waiter can never fall two phases behind:
-//   fullK/fullV[st]  copies landed          (loader -> MMA issuer)
-//   emptyK/emptyV[st] S / P V of the tile done (MMA commit -> loader)
-//   s_bar[b]         S of the tile in buffer b (MMA commit -> softmax)
-//   pv_bar           P V of the tile done     (MMA commit -> softmax)
-//   p_bar            P of the tile written    (256 softmax arrivals -> MMA issuer)
+// Roles: eight softmax warps (one row per thread); lane 0 of one warp issues
+// the S MMAs, of another the TMA copies, of a third the P V MMAs (one warp
+// scheduler each, so the issue loops do not queue behind softmax warps).
+// They meet only at mbarriers, each arranged so that no waiter can fall two
+// phases behind:
+//   fullK/fullV[st]   copies landed              (loader -> S / P V issuers)
+//   emptyK/emptyV[st] S / P V of the tile done   (MMA commits -> loader)
+//   s_bar[b]          S of the tile in buffer b  (S commit -> softmax)
+//   s_free[b]         S buffer b read            (256 softmax arrivals -> S issuer)
+//   pv_bar            P V of the tile done       (P V commit -> softmax)
+//   p_bar             P of the tile written      (256 softmax arrivals -> P V issuer)
 template <int D, int BS>
 __global__ void __launch_bounds__(kTCtaThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -131,11 +137,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   const volatile uint32_t* tmem_slot =
       reinterpret_cast<const volatile uint32_t*>(smem + C::TMEM_OFF);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool softmax = warp < kTMmaWarp;
+  const bool softmax = warp < kTSWarp;
   const int wg = (tid >> 7) & 1, lr = tid & 127;  // warpgroup; row within it = TMEM lane
   const uint32_t fullK = sbase + C::BAR_OFF, fullV = fullK + 8 * kTStages;
   const uint32_t emptyK = fullV + 8 * kTStages, emptyV = emptyK + 8 * kTStages;
   const uint32_t s_bar = emptyV + 8 * kTStages, pv_bar = s_bar + 16, p_bar = pv_bar + 8;
+  const uint32_t s_free = p_bar + 8;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -182,6 +189,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   if (tid == 0) {
     for (int i = 0; i < C::NBARS; ++i) mbar_init(fullK + 8 * i, 1);
     mbar_init(p_bar, kTThreads);  // every softmax thread arrives once per tile
+    mbar_init(s_free, kTThreads);
+    mbar_init(s_free + 8, kTThreads);
     *fault = 0;
     fence_mbarrier_init();
   }
@@ -260,55 +269,59 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       }
     }
     __syncwarp();
-  } else if (warp == kTMmaWarp) {
-    // ---- MMAs, in tile order: S(kt+1) as soon as K(kt+1) has landed (S is
-    // double-buffered in TMEM, so it runs during the softmax of kt), then
-    // P V(kt) once the softmax threads have written P(kt).
-    if (lane == 0 && n_kv > 0) {
-      // Operand descriptors: built once; the start address sits in the low
-      // 14 bits in 16-byte units (shared addresses stay below 2^18), so an
-      // offset into a tile is added to the descriptor directly.
-      const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
-      const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
-      const uint64_t dp = tc_desc_sw128(sbase + C::P_OFF, 16, 1024);
-      const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
+  } else if (warp == kTSWarp || warp == kTPVWarp) {
+    // Operand descriptors: built once; the start address sits in the low 14
+    // bits in 16-byte units (shared addresses stay below 2^18), so an offset
+    // into a tile is added to the low half directly.
+    const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
+    const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
+    const uint64_t dp = tc_desc_sw128(sbase + C::P_OFF, 16, 1024);
+    const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
+    const uint32_t desc_hi = (uint32_t)(dq >> 32);  // identical for dq, dk, dp
+    const uint32_t dv_hi = (uint32_t)(dv >> 32);
+    if (warp == kTSWarp && lane == 0) {
+      // ---- S = Q K^T for both warpgroups, in tile order, double-buffered in
+      // TMEM so that S(kt+1) runs during the softmax of kt
       constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
-      constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
-      auto issue_s = [&](int kt) {  // S_w = Q_w K^T for both warpgroups
+#pragma unroll 1
+      for (int kt = 0; kt < n_kv; ++kt) {
         const int st = kt % kTStages, buf = kt & 1;
+        if (kt >= 2) wait(s_free + 8 * buf, ((kt - 2) >> 1) & 1);  // buffer read by softmax
         wait(fullK + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
-        const uint64_t kb = dk + ((st * C::KV_BYTES) >> 4);
+        const uint32_t klo = (uint32_t)dk + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int w = 0; w < kTWarpgroups; ++w)
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = ((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4;
-            const uint32_t qoff = (w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4;
-            tc_mma_bf16(tmem + tmem_s_col(w, buf), dq + qoff, kb + koff, kIdS, ks > 0);
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc_mma_bf16_lohi(
+                tmem + tmem_s_col(w, buf),
+                (uint32_t)dq + ((w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4), desc_hi,
+                klo + (((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4), desc_hi, kIdS, ks > 0);
         tc_commit(s_bar + 8 * buf);
         tc_commit(emptyK + 8 * st);
-      };
-      issue_s(0);
+      }
+    }
+    if (warp == kTPVWarp && lane == 0) {
+      // ---- O_w += P_hi,w V + P_lo,w V once the softmax has written P(kt)
+      constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
         const int st = kt % kTStages;
-        // S(kt+1)'s buffer was last read by the softmax of kt-1 (p_bar(kt-1))
-        if (kt + 1 < n_kv) issue_s(kt + 1);
-        wait(p_bar, kt & 1);  // P(kt) written, S(kt) read, P V(kt-1) complete
+        wait(p_bar, kt & 1);  // P(kt) written (and P V(kt-1) seen complete)
         wait(fullV + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
-        const uint64_t vb = dv + ((st * C::KV_BYTES) >> 4);
+        const uint32_t vlo = (uint32_t)dv + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int w = 0; w < kTWarpgroups; ++w)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < kTKv / 16; ++ks)
-              tc_mma_bf16(tmem + kTmemO + w * 128,
-                          dp + ((w * C::PWG + part * C::PBUF + ks * 32) >> 4), vb + ks * 128,
-                          kIdPV, !(kt == 0 && part == 0 && ks == 0));
+              tc_mma_bf16_lohi(tmem + kTmemO + w * 128,
+                               (uint32_t)dp + ((w * C::PWG + part * C::PBUF + ks * 32) >> 4),
+                               desc_hi, vlo + ks * 128, dv_hi, kIdPV,
+                               !(kt == 0 && part == 0 && ks == 0));
         tc_commit(pv_bar);
         tc_commit(emptyV + 8 * st);
       }
@@ -336,6 +349,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       tc_ld32(tS + lane_off, sr[0]);
       tc_ld32(tS + lane_off + 32, sr[1]);
       tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free + 8 * (kt & 1));  // the S issuer may refill this buffer
       const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
       const uint64_t vis = lim < 0 ? 0ull : tmask & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
