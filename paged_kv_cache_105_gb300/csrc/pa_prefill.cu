@@ -53,7 +53,7 @@ constexpr int kTRows = 128;                 // M of every MMA: rows per warpgrou
 constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
 constexpr int kTKv = 64;                    // K/V tokens per tile (N of S)
 constexpr int kTUnit = 16;                  // tokens per TMA unit
-constexpr int kTStages = 3;
+constexpr int kTStages = 4;
 // TMEM columns: S of warpgroup w in buffer 0 at 64 w and in buffer 1 at
 // 384 + 64 w; its O at 128 + 128 w
 constexpr uint32_t kTmemCols = 512;
@@ -90,15 +90,12 @@ struct TCfg {
   static constexpr int QHALF = kTRows * 128;              // 16 KB
   static constexpr int QWG = KH * QHALF;                  // one warpgroup's Q
   static constexpr int Q_OFF = 0;
-  static constexpr int PBUF = kTRows * 128;
-  static constexpr int PWG = 2 * PBUF;                    // P hi, then P lo
-  static constexpr int P_OFF = Q_OFF + kTWarpgroups * QWG;
   // K stages [kTStages][KV_BYTES], then V stages: K of a tile is freed by its
   // S, well before its V is freed by its P V, so each streams on its own ring
-  static constexpr int K_OFF = P_OFF + kTWarpgroups * PWG;
+  static constexpr int K_OFF = Q_OFF + kTWarpgroups * QWG;
   static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
-  // fullK[3], fullV[3], emptyK[3], emptyV[3], S done (one per S buffer),
-  // P V done, P written, S read (one per S buffer)
+  // fullK, fullV, emptyK, emptyV (one per stage), S done (one per TMEM
+  // buffer), P V done, P written, buffer free (one per TMEM buffer)
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
   static constexpr int NBARS = 4 * kTStages + 6;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
@@ -120,9 +117,12 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 //   fullK/fullV[st]   copies landed              (loader -> S / P V issuers)
 //   emptyK/emptyV[st] S / P V of the tile done   (MMA commits -> loader)
 //   s_bar[b]          S of the tile in buffer b  (S commit -> softmax)
-//   s_free[b]         S buffer b read            (256 softmax arrivals -> S issuer)
-//   pv_bar            P V of the tile done       (P V commit -> softmax)
 //   p_bar             P of the tile written      (256 softmax arrivals -> P V issuer)
+//   pv_bar            P V of the tile done       (P V commit -> softmax)
+//   b_free[b]         P in buffer b consumed     (P V commit -> S issuer)
+// P overwrites S in its TMEM buffer (hi in the first 32 columns, lo in the
+// next 32, bf16 pairs) and the P V MMA reads it from there, so the softmax of
+// the next tile never waits for this P V except to rescale O.
 template <int D, int BS>
 __global__ void __launch_bounds__(kTCtaThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -142,7 +142,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   const uint32_t fullK = sbase + C::BAR_OFF, fullV = fullK + 8 * kTStages;
   const uint32_t emptyK = fullV + 8 * kTStages, emptyV = emptyK + 8 * kTStages;
   const uint32_t s_bar = emptyV + 8 * kTStages, pv_bar = s_bar + 16, p_bar = pv_bar + 8;
-  const uint32_t s_free = p_bar + 8;
+  const uint32_t b_free = p_bar + 8;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -189,8 +189,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   if (tid == 0) {
     for (int i = 0; i < C::NBARS; ++i) mbar_init(fullK + 8 * i, 1);
     mbar_init(p_bar, kTThreads);  // every softmax thread arrives once per tile
-    mbar_init(s_free, kTThreads);
-    mbar_init(s_free + 8, kTThreads);
+
     *fault = 0;
     fence_mbarrier_init();
   }
@@ -275,7 +274,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     // into a tile is added to the low half directly.
     const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
     const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
-    const uint64_t dp = tc_desc_sw128(sbase + C::P_OFF, 16, 1024);
     const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
     const uint32_t desc_hi = (uint32_t)(dq >> 32);  // identical for dq, dk, dp
     const uint32_t dv_hi = (uint32_t)(dv >> 32);
@@ -286,7 +284,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
         const int st = kt % kTStages, buf = kt & 1;
-        if (kt >= 2) wait(s_free + 8 * buf, ((kt - 2) >> 1) & 1);  // buffer read by softmax
+        if (kt >= 2) wait(b_free + 8 * buf, ((kt - 2) >> 1) & 1);  // P V(kt-2) done
         wait(fullK + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
         const uint32_t klo = (uint32_t)dk + ((st * C::KV_BYTES) >> 4);
@@ -304,6 +302,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     }
     if (warp == kTPVWarp && lane == 0) {
       // ---- O_w += P_hi,w V + P_lo,w V once the softmax has written P(kt)
+      // into the TMEM buffer of S(kt)
       constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
@@ -318,12 +317,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < kTKv / 16; ++ks)
-              tc_mma_bf16_lohi(tmem + kTmemO + w * 128,
-                               (uint32_t)dp + ((w * C::PWG + part * C::PBUF + ks * 32) >> 4),
-                               desc_hi, vlo + ks * 128, dv_hi, kIdPV,
-                               !(kt == 0 && part == 0 && ks == 0));
+              tc_mma_bf16_ta(tmem + kTmemO + w * 128,
+                             tmem + tmem_s_col(w, kt & 1) + part * 32 + ks * 8, vlo + ks * 128,
+                             dv_hi, kIdPV, !(kt == 0 && part == 0 && ks == 0));
         tc_commit(pv_bar);
         tc_commit(emptyV + 8 * st);
+        tc_commit(b_free + 8 * (kt & 1));
       }
     }
     __syncwarp();
@@ -349,8 +348,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       tc_ld32(tS + lane_off, sr[0]);
       tc_ld32(tS + lane_off + 32, sr[1]);
       tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free + 8 * (kt & 1));  // the S issuer may refill this buffer
       const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
       const uint64_t vis = lim < 0 ? 0ull : tmask & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
@@ -394,11 +391,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                                p1 - __uint_as_float(pk[0][k] & 0xffff0000u));
       }
       l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-      // P V(kt-1) must be done before O is rescaled and the P buffers reused
-      if (kt > 0) {
+      // P over S in TMEM: this thread's lane, hi then lo
+      tc_st32(tS + lane_off, pk[0]);
+      tc_st32(tS + lane_off + 32, pk[1]);
+      // O holds earlier tiles: rescale this warp's rows (alpha = 1 for the
+      // others) once P V(kt-1) is done. A warp waits here only when it
+      // rescales; P V(kt) cannot complete before this warp's P(kt) arrival,
+      // so the barrier is never two phases ahead of this wait.
+      if (kt > 0 && warp_need) {
         wait(pv_bar, (kt - 1) & 1);
         tc_fence_after();
-        if (warp_need) {  // rescale this warp's rows of O (alpha = 1 for the others)
+        {
 #pragma unroll
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t o[32];
@@ -411,16 +414,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
           tc_wait_st();
         }
       }
-      uint8_t* ph = smem + C::P_OFF + wg * C::PWG;
-      uint8_t* pl = ph + C::PBUF;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t off = lr * 128 + (((ch ^ lr) & 7) << 4);
-        *reinterpret_cast<uint4*>(ph + off) =
-            make_uint4(pk[0][4 * ch], pk[0][4 * ch + 1], pk[0][4 * ch + 2], pk[0][4 * ch + 3]);
-        *reinterpret_cast<uint4*>(pl + off) =
-            make_uint4(pk[1][4 * ch], pk[1][4 * ch + 1], pk[1][4 * ch + 2], pk[1][4 * ch + 3]);
-      }
+      tc_wait_st();
       if (tmask != ~0ull) {
         // V rows with no token of the sequence may hold anything (even NaN):
         // zero them so that a zero weight times them stays zero (rare: the
@@ -434,14 +428,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                 make_uint4(0, 0, 0, 0);
         }
       }
-      fence_proxy_async_smem();  // P and zeroed rows before the MMA reads them
+      fence_proxy_async_smem();  // zeroed rows before the MMA reads them
       tc_fence_before();
       mbar_arrive(p_bar);
     }
 
     // ---- normalise and write the rows
     if (n_kv > 0) {
-      wait(pv_bar, (n_kv - 1) & 1);  // the last P V
+      // The last P V (and with it every earlier one). Waited on its own
+      // buffer-free barrier: P V(n-2) may still be running, so pv_bar could be
+      // two phases behind this wait, while b_free[(n-1) & 1] has seen
+      // P V(n-3) (S(n-1) waited for it) and has no later phase.
+      wait(b_free + 8 * ((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1);
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll

@@ -62,6 +62,21 @@ __device__ __forceinline__ void tc_mma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo,
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x 16) read from tensor memory, lane =
+// row, each 32-bit column a bf16 pair (lower half = the even k), so one K step
+// of 16 spans 8 columns.
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on the mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
