@@ -62,7 +62,6 @@ constexpr int kMaxSeqs = 8192;
 constexpr int kMaxGrid = 512;                       // persistent CTAs at most
 constexpr int kMaxWorkers = kMaxGrid * 4;           // balanced split: one worker per warp
 constexpr int kMinUnitsPerWorker = 8;               // balanced split: work per warp at least
-constexpr int kMinUnitsPerCta = 16;                 // balanced split: work per CTA at least
 #ifndef PA_PAIR_COST
 #define PA_PAIR_COST 4
 #endif
@@ -78,12 +77,12 @@ struct DecodeArgs {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   // Partials. Fixed partitions: [S][Hq][max_parts] rows. Balanced split:
-  // [kMaxGrid CTAs][2 slots][G heads] rows. O rows have D floats, (m, l) in
-  // log2 units.
+  // [kMaxWorkers warps][2 slots][G heads] rows. O rows have D floats, (m, l)
+  // in log2 units.
   float* ws_o;
   float2* ws_ml;
   int32_t* work;             // [2]: items handed out dynamically, CTAs done
-  int4* pair_info;           // balanced: [S][Hkv] (first CTA, parts, first slot, -)
+  int4* pair_info;           // balanced: [S][Hkv] (first worker, parts, first slot, -)
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
   int part_tokens, max_parts, len_cap;
@@ -633,32 +632,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   const int G = a.group;
   PA_EVENT(1);
 
-  // Fixed partitions: this CTA's items are blockIdx.x, blockIdx.x +
-  // gridDim.x, then one per dynamic fetch (2 * gridDim.x + counter).
-  // Balanced split: the chunks of this CTA's unit range, in order.
+  // This CTA's items are blockIdx.x, blockIdx.x + gridDim.x, then one per
+  // dynamic fetch (2 * gridDim.x + counter).
   int item = blockIdx.x;
-  long long lo = 0, hi = 0, n_ctas = 1, U = 0;
   Item cur{}, nxt{};
   int ids_cur[BOXES], ids_nxt[BOXES];
   uint32_t qf_cur[NT][KS][2], qf_nxt[NT][KS][2];
   bool have_cur, have_nxt = false;
-  if (a.balanced) {
-    U = (long long)a.n_kv * total;  // stream length
-    n_ctas = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
-    if (n_ctas > gridDim.x) n_ctas = gridDim.x;
-    if (n_ctas < 1) n_ctas = 1;
-    lo = (long long)blockIdx.x * U / n_ctas;
-    hi = (long long)(blockIdx.x + 1) * U / n_ctas;
-    have_cur = blockIdx.x < n_ctas && decode_chunk(lo, lo, hi, prefix, lens, a, cur);
-    if (have_cur) have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt);
-  } else {
-    have_cur = item < total;
-    if (have_cur) {
-      cur = decode_item(item, prefix, lens, a);
-      const int item1 = item + (int)gridDim.x;
-      have_nxt = item1 < total;
-      if (have_nxt) nxt = decode_item(item1, prefix, lens, a);
-    }
+  have_cur = item < total;
+  if (have_cur) {
+    cur = decode_item(item, prefix, lens, a);
+    const int item1 = item + (int)gridDim.x;
+    have_nxt = item1 < total;
+    if (have_nxt) nxt = decode_item(item1, prefix, lens, a);
   }
   if (have_cur) {
     load_ids<BS, BOXES, ROWS>(ids_cur, cur, warp, lane, a);
@@ -669,13 +655,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     }
   }
   griddep_wait();  // from here on: pool reads, output and workspace writes
-  if (a.balanced) {
-    // sequences with no tokens own no units: their outputs are zero
-    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
-      if (lens[sq] == 0)
-        for (int i = tid; i < a.n_q * D; i += kThreads)
-          a.out[(int64_t)sq * a.n_q * D + i] = __float2bfloat16_rn(0.f);
-  }
 
   float acc[NT][KS][4];               // this warp's softmax state for the segment
   float mrun[NT][2], lrun[NT][2];
@@ -751,8 +730,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     // ---- fetch item k + 2 of this CTA; the value is only needed after the
     // merge, so it is published then and its latency hides behind the units
     int fetched = INT_MAX;
-    if (tid == 0 && have_nxt && !a.balanced)
-      fetched = 2 * (int)gridDim.x + atomicAdd(&a.work[0], 1);
+    if (tid == 0 && have_nxt) fetched = 2 * (int)gridDim.x + atomicAdd(&a.work[0], 1);
 
     // ---- stream this warp's units of the current chunk
     if (cur.first) {
@@ -806,7 +784,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     }
     fill();  // the next item's first units fly while the CTA merges
     PA_EVENT(3);
-    if (tid == 0 && !a.balanced) {
+    if (tid == 0) {
       mail[k & 3] = fetched;
       mbar_arrive(mail_bar + 8 * (k & 3));
     }
@@ -893,14 +871,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
     PA_EVENT(4);
     const int64_t row0 = (int64_t)cur.s * a.n_q + (int64_t)cur.g * G;
-    if (a.balanced && tid == 0 && cur.holds_first) {
-      // this CTA holds the pair's first unit: tell the merge where its parts are
-      const int w = prefix[cur.s + 1] - prefix[cur.s];
-      const long long B = (long long)a.n_kv * prefix[cur.s] + (long long)(cur.g + 1) * w;
-      const long long c1 = (B * n_ctas - 1) / U;
-      a.pair_info[(int64_t)cur.s * a.n_kv + cur.g] =
-          make_int4(blockIdx.x, (int)(c1 - blockIdx.x + 1), cur.part < 0 ? 0 : cur.part, 0);
-    }
     for (int i = tid; i < G * D; i += kThreads) {
       const int n = i / D, d = i - n * D;
       const float O = macc[n * C::MSTRIDE + d];
@@ -908,8 +878,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       if (cur.part < 0) {
         a.out[(row0 + n) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
       } else {
-        const int64_t wr = a.balanced ? ((int64_t)blockIdx.x * 2 + cur.part) * G + n
-                                      : (row0 + n) * a.max_parts + cur.part;
+        const int64_t wr = (row0 + n) * a.max_parts + cur.part;
         a.ws_o[wr * D + d] = O;
         if (d == 0) a.ws_ml[wr] = make_float2(M, L);
       }
@@ -937,9 +906,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     } else {
       issue_j = 0;
     }
-    if (a.balanced) {
-      have_nxt = decode_chunk(cur.end, lo, hi, prefix, lens, a, nxt);
-    } else {
+    {
       // the new next item is this CTA's item k + 2, fetched at the top of
       // this iteration into mailbox slot k mod 4
       const int slot = k & 3;
@@ -1274,8 +1241,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 // l_p the running max (log2 units) and sum of partition p and O_p its
 // unnormalised output: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
 // M = max_p m_p. Fixed partitions: the parts of a row are its partitions.
-// Balanced split: the parts are the CTAs whose shares cut the row's
-// (sequence, kv head) pair, as recorded by the CTA holding its first unit.
+// Balanced split: the parts are the warps whose shares cut the row's
+// (sequence, kv head) pair, as recorded by the warp holding its first unit.
 struct MergeArgs {
   __nv_bfloat16* out;
   const float* ws_o;
@@ -1300,7 +1267,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
     int nparts;
     long long rbase, rfirst, rstep;  // row of part q: q == 0 ? rfirst : rbase + q * rstep
     if (m.balanced) {
-      // Balanced split: parts are CTAs c0 .. c0 + n - 1; CTA c keeps slot
+      // Balanced split: parts are warps c0 .. c0 + n - 1; warp c keeps slot
       // (2c + slot) * G + head; only c0 may use slot 1.
       const int h = row - s * m.n_q, g = h / m.group, n = h - g * m.group;
       const int4 pi = __ldcg(&m.pair_info[(int64_t)s * m.n_kv + g]);

@@ -160,6 +160,16 @@ def test_one_long_sequence_among_short_ones(mode):
     full_parity(wl, partition_tokens=0 if mode == "balanced" else 256)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 2, 64), (12, 4, 128), (8, 8, 128)])
+def test_balanced_split_pair_cut_into_many_pieces(hq, hkv, d):
+    # a pair spread over far more than 16 warps: its pieces are combined in
+    # groups first, then the groups (the in-kernel two-level merge)
+    wl = W.custom([3, 25000, 17, 1], block_size=16, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                  seed=hq + d)
+    (a, r), _, _ = full_parity(wl, partition_tokens=0)
+    assert a < 1e-2 and r < 2e-2
+
+
 def test_block_placement_does_not_matter():
     base = W.custom([900, 33, 1500], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128,
                     seed=21)
