@@ -459,12 +459,13 @@ def run_prefill(args):
                        "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
                        "head_dim": wl.head_dim, "block_size": wl.block_size,
                        "flops_per_step": flops, "kv_bytes": wl.kv_bytes(),
-                       "arithmetic": "bf16 mma.sync m16n8k16, fp32 accumulation; P as a "
-                                     "bf16 hi + lo pair, so the P V product runs twice",
+                       "arithmetic": "bf16 tcgen05.mma (M 128), fp32 accumulation in TMEM; "
+                                     "P as a bf16 hi + lo pair read from TMEM, so the P V "
+                                     "product runs twice",
                        "launch": "one CUDA graph replay per step (write, prefill)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                         "kernel": "prefill_kernel (pa_prefill)",
+                         "kernel": "prefill_tc_kernel (pa_prefill)",
                          "peak_source": f"{kind} bf16_tflops (cuBLAS, burst)",
                          "prefill_ms_avg": att_ms},
             "gpu_launches": 2 * args.steps, "clocks": clk}
