@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32])
     p.add_argument("--partition-tokens", type=int, default=None)
+    p.add_argument("--num-seqs", type=int, default=None,
+                   help="configs 2-5: a smaller batch of the same shape (profiling)")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
@@ -61,10 +63,17 @@ def parse():
     return p.parse_args()
 
 
-def build_workload(cfg, bs):
+def build_workload(cfg, bs, num_seqs=None):
+    """Config `cfg`; num_seqs shrinks configs 2-5 to a smaller batch of the
+    same shape (for profiling captures that must stay small)."""
     from paged_kv_cache_105_gb300 import workloads as W
+    kw = {} if num_seqs is None else {"num_seqs": num_seqs}
+    if num_seqs is not None and cfg not in (2, 3, 4, 5):
+        raise SystemExit("--num-seqs applies to configs 2-5")
     if cfg == 3:
-        return W.config3(block_size=bs)
+        return W.config3(block_size=bs, **kw)
+    if kw:
+        return {2: W.config2, 4: W.config4, 5: W.config5}[cfg](**kw)
     return W.CONFIGS[cfg]()
 
 
@@ -218,7 +227,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = build_workload(args.config, args.block_size)
+    wl = build_workload(args.config, args.block_size, args.num_seqs)
     if hasattr(wl, "steps"):  # multi-step workload: the oracle times its first step
         wl = wl.steps[0]
     budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
@@ -306,7 +315,7 @@ def run_swap(args):
     __graft_entry__.build()
     from paged_kv_cache_105_gb300 import binding as B
     from paged_kv_cache_105_gb300 import workloads as W
-    wl = build_workload(args.config, args.block_size)
+    wl = build_workload(args.config, args.block_size, args.num_seqs)
     fp8 = fp8_scale_of(args)
     vals = W.make_values_fp8(wl, device=dev) if fp8 is not None else W.make_values(wl, device=dev)
     gk, gv = vals["k_pool"], vals["v_pool"]
@@ -499,7 +508,7 @@ def main():
     # A workload is a list of decode steps over one pool: one step for the
     # single-step batches, T steps (forks, frees, copy-on-write between them)
     # for beam search; the timed steps cycle through them.
-    wl0 = build_workload(args.config, args.block_size)
+    wl0 = build_workload(args.config, args.block_size, args.num_seqs)
     multi = isinstance(wl0, W.MultiStep)
     steps_wl = wl0.steps if multi else [wl0]
     wl = steps_wl[0]
