@@ -66,6 +66,8 @@ class PAError(RuntimeError):
 def lib():
     """The loaded ``libpa.so``; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_build.LIB):
@@ -81,14 +83,24 @@ def lib():
     return _lib
 
 
+# The argument types are declared (SIGNATURES), so ctypes takes plain ints
+# for the pointer arguments; these helpers stay cheap because every step of
+# a serving loop goes through them.
 def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+# The raw current stream of a device, without building a Stream object.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream, device):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(device.index if device.index is not None else
+                               torch.cuda.current_device())
         stream = torch.cuda.current_stream(device)
-    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _check(t, name, dtype, dim=None, device=None):
@@ -98,7 +110,7 @@ def _check(t, name, dtype, dim=None, device=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if device is not None and t.device != device:
+    if device is not None and t.get_device() != device.index:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
