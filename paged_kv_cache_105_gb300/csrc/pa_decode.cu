@@ -114,11 +114,11 @@ struct Cfg {
   static constexpr int MAIL_OFF = BAR_OFF + NBARS * 8;
   static constexpr int MISC_OFF = MAIL_OFF + 16;
   static constexpr int FIN_OFF = MISC_OFF + 32;      // 2 x 16 floats
-  static constexpr int ML_OFF = FIN_OFF + 2 * 16 * 4;  // 3 warps x HEADS x (m, l)
-  static constexpr int MERGE_OFF = ML_OFF + 3 * HEADS * 2 * 4;
-  // Merge buffer: 3 warps x G heads x MSTRIDE floats; then the prefix table.
+  static constexpr int ML_OFF = FIN_OFF + 2 * 16 * 4;  // 2 slots x HEADS x (m, l)
+  static constexpr int MERGE_OFF = ML_OFF + 2 * HEADS * 2 * 4;
+  // Merge buffer: 2 slots x G heads x MSTRIDE floats; then the prefix table.
   __host__ __device__ static int prefix_off(int group) {
-    return MERGE_OFF + 3 * group * MSTRIDE * 4;
+    return MERGE_OFF + 2 * group * MSTRIDE * 4;
   }
   // prefix[num_seqs + 1] then the clamped lengths lens[num_seqs]
   static size_t smem_bytes(int num_seqs, int group) {
@@ -796,9 +796,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       lrun[t][1] = warp_sum_xor4(lrun[t][1]);
     }
 
-    // ---- merge: warps 1-3 hand their state to warp 0 through shared memory
-    if (warp > 0) {
-      float* buf = macc + (warp - 1) * G * C::MSTRIDE;
+    // ---- merge: the four warps' states meet in two rounds through two
+    // shared-memory slots (warps 2, 3 -> 0, 1, then 1 -> 0), so that the
+    // buffer holds two warps' rows, not three
+    auto put = [&](int slot) {
+      float* buf = macc + slot * G * C::MSTRIDE;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -813,39 +815,44 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
             const int n = t * 8 + 2 * lane + jj;
-            mlb[((warp - 1) * C::HEADS + n) * 2] = mrun[t][jj];
-            mlb[((warp - 1) * C::HEADS + n) * 2 + 1] = lrun[t][jj];
+            mlb[(slot * C::HEADS + n) * 2] = mrun[t][jj];
+            mlb[(slot * C::HEADS + n) * 2 + 1] = lrun[t][jj];
           }
         }
       }
-    }
+    };
+    auto take = [&](int slot) {
+      const float* buf = macc + slot * G * C::MSTRIDE;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int n = t * 8 + 2 * (lane & 3) + jj;
+          if (n >= G) continue;
+          const float mo = mlb[(slot * C::HEADS + n) * 2];
+          const float lo = mlb[(slot * C::HEADS + n) * 2 + 1];
+          const float M = fmaxf(mrun[t][jj], mo);
+          const float es = mrun[t][jj] == -INFINITY ? 0.f : fast_exp2(mrun[t][jj] - M);
+          const float eo = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+          lrun[t][jj] = es * lrun[t][jj] + eo * lo;
+          mrun[t][jj] = M;
+#pragma unroll
+          for (int dt = 0; dt < KS; ++dt) {
+            const int d = dt * 16 + (lane >> 2);
+            acc[t][dt][jj] = es * acc[t][dt][jj] + eo * buf[n * C::MSTRIDE + d];
+            acc[t][dt][jj + 2] = es * acc[t][dt][jj + 2] + eo * buf[n * C::MSTRIDE + d + 8];
+          }
+        }
+      }
+    };
+    if (warp >= 2) put(warp - 2);
+    __syncthreads();
+    if (warp < 2) take(warp);
+    __syncthreads();
+    if (warp == 1) put(0);
     __syncthreads();
     if (warp == 0) {
-#pragma unroll 1
-      for (int w = 0; w < kWarps - 1; ++w) {
-        const float* buf = macc + w * G * C::MSTRIDE;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int n = t * 8 + 2 * (lane & 3) + jj;
-            if (n >= G) continue;
-            const float mo = mlb[(w * C::HEADS + n) * 2];
-            const float lo = mlb[(w * C::HEADS + n) * 2 + 1];
-            const float M = fmaxf(mrun[t][jj], mo);
-            const float es = mrun[t][jj] == -INFINITY ? 0.f : fast_exp2(mrun[t][jj] - M);
-            const float eo = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
-            lrun[t][jj] = es * lrun[t][jj] + eo * lo;
-            mrun[t][jj] = M;
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-              const int d = dt * 16 + (lane >> 2);
-              acc[t][dt][jj] = es * acc[t][dt][jj] + eo * buf[n * C::MSTRIDE + d];
-              acc[t][dt][jj + 2] = es * acc[t][dt][jj + 2] + eo * buf[n * C::MSTRIDE + d + 8];
-            }
-          }
-        }
-      }
+      take(0);
       // the CTA's result for the item, back into buffer 0 for coalesced writes
       float* buf = macc;
 #pragma unroll
