@@ -17,14 +17,14 @@
 //    128-byte-swizzled K-major layout the MMA reads.
 //  * K/V stream in tiles of 64 tokens (four 16-token units, the decode's TMA
 //    boxes, each 64-column half of a row stored as its own 64-row slab)
-//    through a 3-stage ring filled by TMA.
+//    through 4-stage rings (K and V separately) filled by TMA.
 //  * Per tile: S = Q K^T (M 128, N 64, both operands K-major) into TMEM;
 //    every thread loads its row of S, masks it (causal, length, bad blocks),
 //    runs the online softmax in base 2 with a lazily moved reference
 //    (rescaling its row of O in TMEM in the rare case the reference moves),
-//    and writes P to shared memory as a bf16 pair hi + lo; then
-//    O += P_hi V + P_lo V (M 128, N head_dim, V read MN-major) accumulates in
-//    TMEM. One thread issues the MMAs. S is double-buffered in TMEM: S of the
+//    and writes P over its S in TMEM as a bf16 pair hi + lo; then
+//    O += P_hi V + P_lo V (M 128, N head_dim, A = P from TMEM, V read
+//    MN-major) accumulates in TMEM. S is double-buffered in TMEM: S of the
 //    next tile and P V of the previous one run on the tensor cores while the
 //    threads compute the softmax of the current one.
 //  * O is normalised and written as bf16 after the last tile.
@@ -227,7 +227,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   };
 
   if (warp == kTLoadWarp) {
-    // ---- copies: K and V of every tile through their 3-stage rings
+    // ---- copies: K and V of every tile through their rings
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
@@ -428,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                 make_uint4(0, 0, 0, 0);
         }
       }
-      fence_proxy_async_smem();  // zeroed rows before the MMA reads them
+      if (tmask != ~0ull) fence_proxy_async_smem();  // zeroed rows before the MMA reads them
       tc_fence_before();
       mbar_arrive(p_bar);
     }
