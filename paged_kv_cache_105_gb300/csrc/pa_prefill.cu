@@ -269,33 +269,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     }
     __syncwarp();
   } else if (warp == kTSWarp || warp == kTPVWarp) {
-    // Operand descriptors: built once; the start address sits in the low 14
-    // bits in 16-byte units (shared addresses stay below 2^18), so an offset
-    // into a tile is added to the low half directly.
+    // Operand descriptors: the start address sits in the low 14 bits in
+    // 16-byte units (shared addresses stay below 2^18), so an offset into a
+    // tile is added to the descriptor directly.
     const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
     const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
     const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
-    const uint32_t desc_hi = (uint32_t)(dq >> 32);  // identical for dq, dk, dp
-    const uint32_t dv_hi = (uint32_t)(dv >> 32);
     if (warp == kTSWarp && lane == 0) {
       // ---- S = Q K^T for both warpgroups, in tile order, double-buffered in
-      // TMEM so that S(kt+1) runs during the softmax of kt
+      // TMEM so that S(kt+1) runs during the softmax of kt. Q's descriptors
+      // are fixed and K's are formed once per tile, so that each MMA issues
+      // on its own (the issuing lane shares its scheduler with two softmax
+      // warps).
       constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
+      uint64_t dqs[kTWarpgroups][D / 16];
+#pragma unroll
+      for (int w = 0; w < kTWarpgroups; ++w)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          dqs[w][ks] = dq + ((w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4);
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
         const int st = kt % kTStages, buf = kt & 1;
+        uint64_t dks[D / 16];
+        const uint64_t dk_st = dk + ((st * C::KV_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          dks[ks] = dk_st + (((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4);
+        const uint32_t d0 = tmem + tmem_s_col(0, buf), d1 = tmem + tmem_s_col(1, buf);
         if (kt >= 2) wait(b_free + 8 * buf, ((kt - 2) >> 1) & 1);  // P V(kt-2) done
         wait(fullK + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
-        const uint32_t klo = (uint32_t)dk + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int w = 0; w < kTWarpgroups; ++w)
+        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d0, dqs[0][ks], dks[ks], kIdS, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            tc_mma_bf16_lohi(
-                tmem + tmem_s_col(w, buf),
-                (uint32_t)dq + ((w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4), desc_hi,
-                klo + (((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4), desc_hi, kIdS, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d1, dqs[1][ks], dks[ks], kIdS, ks > 0);
         tc_commit(s_bar + 8 * buf);
         tc_commit(emptyK + 8 * st);
       }
@@ -307,19 +315,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
         const int st = kt % kTStages;
+        uint64_t dvs[kTKv / 16];  // V's descriptors of this tile, formed before the waits
+        const uint64_t dv_st = dv + ((st * C::KV_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kTKv / 16; ++ks) dvs[ks] = dv_st + ks * 128;
+        const uint32_t a0 = tmem + tmem_s_col(0, kt & 1), a1 = tmem + tmem_s_col(1, kt & 1);
+        const uint32_t first = kt == 0;
         wait(p_bar, kt & 1);  // P(kt) written (and P V(kt-1) seen complete)
         wait(fullV + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
-        const uint32_t vlo = (uint32_t)dv + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int w = 0; w < kTWarpgroups; ++w)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < kTKv / 16; ++ks)
-              tc_mma_bf16_ta(tmem + kTmemO + w * 128,
-                             tmem + tmem_s_col(w, kt & 1) + part * 32 + ks * 8, vlo + ks * 128,
-                             dv_hi, kIdPV, !(kt == 0 && part == 0 && ks == 0));
+              tc_mma_bf16_ta64(tmem + kTmemO + w * 128, (w ? a1 : a0) + part * 32 + ks * 8,
+                               dvs[ks], kIdPV, (part | ks) ? 1u : !first);
         tc_commit(pv_bar);
         tc_commit(emptyV + 8 * st);
         tc_commit(b_free + 8 * (kt & 1));

@@ -77,6 +77,16 @@ __device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// tc_mma_bf16_ta with the B descriptor whole.
+__device__ __forceinline__ void tc_mma_bf16_ta64(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive on the mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
