@@ -43,11 +43,11 @@ namespace {
 
 constexpr int kTWarpgroups = 2;             // each owns 128 rows (one MMA M)
 constexpr int kTThreads = 128 * kTWarpgroups;  // softmax threads, one per row
-// then three single-lane roles, each on its own warp scheduler: S = Q K^T
-// issue, TMA copies, P V issue
-constexpr int kTSWarp = kTThreads / 32;
-constexpr int kTLoadWarp = kTSWarp + 1;
-constexpr int kTPVWarp = kTSWarp + 2;
+// then three single-lane roles, each on its own warp scheduler: the MMA
+// issuer of warpgroup 0, the TMA copies, the MMA issuer of warpgroup 1
+constexpr int kTIssue0Warp = kTThreads / 32;
+constexpr int kTLoadWarp = kTIssue0Warp + 1;
+constexpr int kTIssue1Warp = kTIssue0Warp + 2;
 constexpr int kTCtaThreads = kTThreads + 96;
 constexpr int kTRows = 128;                 // M of every MMA: rows per warpgroup
 constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
@@ -94,10 +94,10 @@ struct TCfg {
   // S, well before its V is freed by its P V, so each streams on its own ring
   static constexpr int K_OFF = Q_OFF + kTWarpgroups * QWG;
   static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
-  // fullK, fullV, emptyK, emptyV (one per stage), S done (one per TMEM
-  // buffer), P V done, P written, buffer free (one per TMEM buffer)
+  // fullK, fullV, emptyK, emptyV (one per stage); per warpgroup: S done
+  // (one per TMEM buffer), P written, P V done, buffer free (one per buffer)
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
-  static constexpr int NBARS = 4 * kTStages + 6;
+  static constexpr int NBARS = 4 * kTStages + 6 * kTWarpgroups;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
   static constexpr size_t SMEM = 1024 + FAULT_OFF + 8;
@@ -110,16 +110,19 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 }
 
 // Roles: eight softmax warps (one row per thread); lane 0 of one warp issues
-// the S MMAs, of another the TMA copies, of a third the P V MMAs (one warp
-// scheduler each, so the issue loops do not queue behind softmax warps).
-// They meet only at mbarriers, each arranged so that no waiter can fall two
-// phases behind:
-//   fullK/fullV[st]   copies landed              (loader -> S / P V issuers)
-//   emptyK/emptyV[st] S / P V of the tile done   (MMA commits -> loader)
-//   s_bar[b]          S of the tile in buffer b  (S commit -> softmax)
-//   p_bar             P of the tile written      (256 softmax arrivals -> P V issuer)
-//   pv_bar            P V of the tile done       (P V commit -> softmax)
-//   b_free[b]         P in buffer b consumed     (P V commit -> S issuer)
+// the MMAs of warpgroup 0, of another those of warpgroup 1, of a third the
+// TMA copies (one warp scheduler each). Each warpgroup runs its own pipeline,
+// S(kt) -> softmax(kt) -> P V(kt) -> S(kt + 2), so the tensor cores work for
+// one warpgroup while the other computes its softmax; they share only the
+// K/V stages. The roles meet only at mbarriers, each arranged so that no
+// waiter can fall two phases behind:
+//   fullK/fullV[st]     copies landed               (loader -> both issuers)
+//   emptyK/emptyV[st]   S / P V of the tile done    (2 MMA commits -> loader)
+// and, per warpgroup w,
+//   s_bar[w][b]         S_w of the tile in buffer b (S commit -> softmax w)
+//   p_bar[w]            P_w of the tile written     (128 arrivals -> issuer w)
+//   pv_bar[w]           P V_w of the tile done      (P V commit -> softmax w)
+//   b_free[w][b]        P_w in buffer b consumed    (P V commit -> issuer w, softmax w)
 // P overwrites S in its TMEM buffer (hi in the first 32 columns, lo in the
 // next 32, bf16 pairs) and the P V MMA reads it from there, so the softmax of
 // the next tile never waits for this P V except to rescale O.
@@ -137,12 +140,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   const volatile uint32_t* tmem_slot =
       reinterpret_cast<const volatile uint32_t*>(smem + C::TMEM_OFF);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool softmax = warp < kTSWarp;
+  const bool softmax = warp < kTIssue0Warp;
   const int wg = (tid >> 7) & 1, lr = tid & 127;  // warpgroup; row within it = TMEM lane
   const uint32_t fullK = sbase + C::BAR_OFF, fullV = fullK + 8 * kTStages;
   const uint32_t emptyK = fullV + 8 * kTStages, emptyV = emptyK + 8 * kTStages;
-  const uint32_t s_bar = emptyV + 8 * kTStages, pv_bar = s_bar + 16, p_bar = pv_bar + 8;
-  const uint32_t b_free = p_bar + 8;
+  // per warpgroup w: s_bar[w][b] at s_bar0 + 16 w + 8 b, p_bar[w] at
+  // p_bar0 + 8 w, pv_bar[w] at pv_bar0 + 8 w, b_free[w][b] at b_free0 + 16 w + 8 b
+  const uint32_t s_bar0 = emptyV + 8 * kTStages, p_bar0 = s_bar0 + 16 * kTWarpgroups;
+  const uint32_t pv_bar0 = p_bar0 + 8 * kTWarpgroups, b_free0 = pv_bar0 + 8 * kTWarpgroups;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -188,7 +193,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   if (warp == 0) tc_alloc(sbase + C::TMEM_OFF, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < C::NBARS; ++i) mbar_init(fullK + 8 * i, 1);
-    mbar_init(p_bar, kTThreads);  // every softmax thread arrives once per tile
+    for (int st = 0; st < kTStages; ++st) {  // one commit from each issuer
+      mbar_init(emptyK + 8 * st, kTWarpgroups);
+      mbar_init(emptyV + 8 * st, kTWarpgroups);
+    }
+    for (int w = 0; w < kTWarpgroups; ++w)
+      mbar_init(p_bar0 + 8 * w, 128);  // every thread of warpgroup w, once per tile
 
     *fault = 0;
     fence_mbarrier_init();
@@ -268,79 +278,80 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       }
     }
     __syncwarp();
-  } else if (warp == kTSWarp || warp == kTPVWarp) {
+  } else if (warp == kTIssue0Warp || warp == kTIssue1Warp) {
+    // ---- the MMAs of warpgroup w, issued by one lane:
+    // S_w(0), S_w(1), then per tile P V_w(kt) and S_w(kt + 2).
+    // S_w(kt) = Q_w K(kt)^T goes into buffer kt & 1 of the warpgroup's S
+    // (double-buffered, so S_w(kt+1) is ready when the softmax of kt ends);
+    // O_w += P_hi V + P_lo V once the softmax has written P_w(kt) over S_w(kt).
     // Operand descriptors: the start address sits in the low 14 bits in
     // 16-byte units (shared addresses stay below 2^18), so an offset into a
-    // tile is added to the descriptor directly.
-    const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF, 16, 1024);
-    const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
-    const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
-    if (warp == kTSWarp && lane == 0) {
-      // ---- S = Q K^T for both warpgroups, in tile order, double-buffered in
-      // TMEM so that S(kt+1) runs during the softmax of kt. Q's descriptors
-      // are fixed and K's are formed once per tile, so that each MMA issues
-      // on its own (the issuing lane shares its scheduler with two softmax
-      // warps).
+    // tile is added to the descriptor directly; they are formed before the
+    // waits, so that each MMA issues on its own (the issuing lane shares its
+    // scheduler with two softmax warps).
+    const int w = warp == kTIssue0Warp ? 0 : 1;
+    if (lane == 0) {
+      const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF + w * C::QWG, 16, 1024);
+      const uint64_t dk = tc_desc_sw128(sbase + C::K_OFF, 16, 1024);
+      const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
       constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
-      uint64_t dqs[kTWarpgroups][D / 16];
+      constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
+      const uint32_t s_bar = s_bar0 + 16 * w, b_free = b_free0 + 16 * w;
+      uint64_t dqs[D / 16];
 #pragma unroll
-      for (int w = 0; w < kTWarpgroups; ++w)
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          dqs[w][ks] = dq + ((w * C::QWG + (ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4);
-#pragma unroll 1
-      for (int kt = 0; kt < n_kv; ++kt) {
+      for (int ks = 0; ks < D / 16; ++ks)
+        dqs[ks] = dq + (((ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4);
+      auto issue_s = [&](int kt) {
         const int st = kt % kTStages, buf = kt & 1;
         uint64_t dks[D / 16];
         const uint64_t dk_st = dk + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           dks[ks] = dk_st + (((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4);
-        const uint32_t d0 = tmem + tmem_s_col(0, buf), d1 = tmem + tmem_s_col(1, buf);
-        if (kt >= 2) wait(b_free + 8 * buf, ((kt - 2) >> 1) & 1);  // P V(kt-2) done
+        const uint32_t d = tmem + tmem_s_col(w, buf);
+        if (kt >= 2) wait(b_free + 8 * buf, ((kt - 2) >> 1) & 1);  // P V_w(kt-2) done
         wait(fullK + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d0, dqs[0][ks], dks[ks], kIdS, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d1, dqs[1][ks], dks[ks], kIdS, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d, dqs[ks], dks[ks], kIdS, ks > 0);
         tc_commit(s_bar + 8 * buf);
         tc_commit(emptyK + 8 * st);
-      }
-    }
-    if (warp == kTPVWarp && lane == 0) {
-      // ---- O_w += P_hi,w V + P_lo,w V once the softmax has written P(kt)
-      // into the TMEM buffer of S(kt)
-      constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
-#pragma unroll 1
-      for (int kt = 0; kt < n_kv; ++kt) {
+      };
+      auto issue_pv = [&](int kt) {
         const int st = kt % kTStages;
-        uint64_t dvs[kTKv / 16];  // V's descriptors of this tile, formed before the waits
+        uint64_t dvs[kTKv / 16];
         const uint64_t dv_st = dv + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kTKv / 16; ++ks) dvs[ks] = dv_st + ks * 128;
-        const uint32_t a0 = tmem + tmem_s_col(0, kt & 1), a1 = tmem + tmem_s_col(1, kt & 1);
+        const uint32_t a = tmem + tmem_s_col(w, kt & 1), o = tmem + kTmemO + w * 128;
         const uint32_t first = kt == 0;
-        wait(p_bar, kt & 1);  // P(kt) written (and P V(kt-1) seen complete)
+        wait(p_bar0 + 8 * w, kt & 1);  // P_w(kt) written (and P V_w(kt-1) seen complete)
         wait(fullV + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
 #pragma unroll
-        for (int w = 0; w < kTWarpgroups; ++w)
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < kTKv / 16; ++ks)
-              tc_mma_bf16_ta64(tmem + kTmemO + w * 128, (w ? a1 : a0) + part * 32 + ks * 8,
-                               dvs[ks], kIdPV, (part | ks) ? 1u : !first);
-        tc_commit(pv_bar);
+          for (int ks = 0; ks < kTKv / 16; ++ks)
+            tc_mma_bf16_ta64(o, a + part * 32 + ks * 8, dvs[ks], kIdPV,
+                             (part | ks) ? 1u : !first);
+        tc_commit(pv_bar0 + 8 * w);
         tc_commit(emptyV + 8 * st);
         tc_commit(b_free + 8 * (kt & 1));
+      };
+      if (n_kv > 0) issue_s(0);
+      if (n_kv > 1) issue_s(1);
+#pragma unroll 1
+      for (int kt = 0; kt < n_kv; ++kt) {
+        issue_pv(kt);
+        if (kt + 2 < n_kv) issue_s(kt + 2);
       }
     }
     __syncwarp();
   } else {
-    // ---- the softmax warps: one row per thread
+    // ---- the softmax warps: one row per thread, on warpgroup wg's barriers
     const uint32_t tO = tmem + kTmemO + wg * 128;
+    const uint32_t s_bar = s_bar0 + 16 * wg, p_bar = p_bar0 + 8 * wg;
+    const uint32_t pv_bar = pv_bar0 + 8 * wg, b_free = b_free0 + 16 * wg;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float m = -INFINITY, l = 0.f;
     int ids_nxt[NB];
@@ -430,10 +441,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       if (tmask != ~0ull) {
         // V rows with no token of the sequence may hold anything (even NaN):
         // zero them so that a zero weight times them stays zero (rare: the
-        // sequence's last tile or a bad block)
+        // sequence's last tile or a bad block). Each warpgroup zeroes every
+        // such row itself, since its P V waits only for its own threads (the
+        // other warpgroup writes the same zeros).
         wait(fullV + 8 * st, (kt / kTStages) & 1);
         uint8_t* vb = smem + C::V_OFF + st * C::KV_BYTES;
-        for (int i = tid; i < kTKv * C::KH * 8; i += kTThreads) {
+        for (int i = lr; i < kTKv * C::KH * 8; i += 128) {
           const int r = i / (C::KH * 8), rest = i % (C::KH * 8), h = rest / 8, ch = rest % 8;
           if (!(tmask >> r & 1))
             *reinterpret_cast<uint4*>(vb + h * C::HALF + r * 128 + ch * 16) =
