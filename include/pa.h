@@ -125,8 +125,8 @@ size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads, int n_kv_heads, in
  * partitions of that many tokens, processed in parallel. With
  * partition_tokens == 0 (the default) the 16-token units of all (sequence,
  * kv head) pairs, taken in order, are cut into equal contiguous shares, one
- * per CTA, so every CTA streams the same number of bytes whatever the
- * length mix. Either way partial results are merged with a log-sum-exp
+ * per warp of a persistent grid, so every warp streams the same number of
+ * bytes whatever the length mix. Either way partial results are merged with a log-sum-exp
  * reduction (the same value as unsplit attention, up to fp32 rounding). The call
  * launches the decode kernel and, when partials need merging, a merge kernel
  * after it. Both are programmatic dependent launches. The decode kernel may
