@@ -89,6 +89,25 @@ def dist_init(args):
     return ws, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest x over the ranks: the job takes as long as its slowest
+    rank. Collective: every rank calls it, with world > 1 under an initialised
+    process group (NCCL on the GPUs; gloo works for CPU tensors)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units all ranks processed per second: each of the `world` replicas does
+    the same work, and `seconds` is the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -358,10 +377,11 @@ def run_swap(args):
     clk = clocks.stop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
+    res = {k: max_over_ranks(v, world, dev) for k, v in res.items()}
     if rank != 0:
         return
-    gbs = moved / (res["kernel"] * 1e-3) / 1e9
-    ce = moved / (res["copy_engine"] * 1e-3) / 1e9
+    gbs = whole_job_rate(moved, world, res["kernel"] * 1e-3) / 1e9
+    ce = whole_job_rate(moved, world, res["copy_engine"] * 1e-3) / 1e9
     line = {"metric": "KV block swap, device <-> pinned host (out + in) GB/s", "value": gbs,
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": res["kernel"], "higher_is_better": True, "scaling": "weak",
@@ -445,12 +465,12 @@ def run_prefill(args):
     clk = clocks.stop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
+    step_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    att_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
     if rank != 0:
         return
-    step_ms = e0.elapsed_time(e1) / args.steps
-    att_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
     flops = wl.flops()
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, step_ms * 1e-3) / 1e12
     achieved = flops / (att_ms * 1e-3) / 1e12
     peak, kind = None, "fallback"
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -667,13 +687,8 @@ def main():
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
 
-    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
 
     timed = [steps_wl[i % T] for i in range(args.steps)]
     kv_total = sum(w.kv_bytes(eb) for w in timed)
@@ -682,8 +697,8 @@ def main():
     alg_bytes = alg_total / args.steps
     tok_total = sum(w.tokens_attended for w in timed)
     ms_per_step = total_ms / args.steps
-    value = world * kv_total / (total_ms * 1e-3) / 1e9
-    tokens_per_s = world * tok_total / (total_ms * 1e-3)
+    value = whole_job_rate(kv_total, world, total_ms * 1e-3) / 1e9
+    tokens_per_s = whole_job_rate(tok_total, world, total_ms * 1e-3)
 
     # ---- end to end through the public API, host buffers, copies timed
     e2e_steps = args.e2e_steps or max(10, min(200, args.steps))
@@ -738,13 +753,9 @@ def main():
         h2d_steps.append(e2e_step(i))
     w1 = time.perf_counter()
     barrier()
-    e2e_s = w1 - w0
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = world * sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)) / e2e_s / 1e9
+    e2e_s = max_over_ranks(w1 - w0, world, dev)
+    e2e_value = whole_job_rate(sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)),
+                               world, e2e_s) / 1e9
     h2d = sum(h2d_steps) / len(h2d_steps)
 
     if rank != 0:
