@@ -201,29 +201,43 @@ def _bits(t):
     return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def cpu_oracle_step(wl, vals_cpu, seqs, fp8_scale=None):
+def cpu_oracle_step(wl, vals_cpu, seqs, fp8_scale=None, threads=1):
     """The oracle's copy -> write -> attention for the sequences `seqs`
     (a bounded sample of the workload); fp8_scale: E4M3 pools with that
-    scale for K and V. Returns KV bytes of the sample."""
+    scale for K and V. threads > 1: the attention's (sequence, head) rows are
+    split across that many threads (the oracle's calls release the GIL).
+    Returns KV bytes of the sample."""
     import numpy as np
     from oracle import paref
     bits = _bits
     rows = np.array([(s, h) for s in seqs for h in range(wl.n_q_heads)], np.int32)
+    if threads > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        chunks = [c for c in np.array_split(rows, threads) if len(c)]
+        attend = paref.attention_paged_fp8 if fp8_scale is not None else paref.attention_paged
+        extra = (fp8_scale, fp8_scale) if fp8_scale is not None else ()
+
+        def attention(q, kp, vp, bt, sl, scale, *sc, rows):
+            with ThreadPoolExecutor(len(chunks)) as ex:
+                list(ex.map(lambda c: attend(q, kp, vp, bt, sl, scale, *sc, rows=c), chunks))
+    else:
+        attention = None
     ntok = int(wl.seq_lens[list(seqs)].astype(np.int64).sum())
     if fp8_scale is not None:
         kp, vp = vals_cpu["k_pool"].numpy().copy(), vals_cpu["v_pool"].numpy().copy()
         paref.copy_blocks(kp.view(np.uint16), vp.view(np.uint16), wl.cow_pairs)
         paref.reshape_and_cache_fp8(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
                                     wl.slot_mapping, fp8_scale, fp8_scale)
-        paref.attention_paged_fp8(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
-                                  wl.scale, fp8_scale, fp8_scale, rows=rows)
+        (attention or paref.attention_paged_fp8)(bits(vals_cpu["q"]), kp, vp, wl.block_tables,
+                                                 wl.seq_lens, wl.scale, fp8_scale, fp8_scale,
+                                                 rows=rows)
         return ntok * wl.n_kv_heads * wl.head_dim * 1 * 2
     kp, vp = bits(vals_cpu["k_pool"]).copy(), bits(vals_cpu["v_pool"]).copy()
     paref.copy_blocks(kp, vp, wl.cow_pairs)
     paref.reshape_and_cache(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
                             wl.slot_mapping)
-    paref.attention_paged(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
-                          wl.scale, rows=rows)
+    (attention or paref.attention_paged)(bits(vals_cpu["q"]), kp, vp, wl.block_tables,
+                                         wl.seq_lens, wl.scale, rows=rows)
     return ntok * wl.n_kv_heads * wl.head_dim * 2 * 2
 
 
@@ -797,6 +811,21 @@ def main():
                "sample": f"{len(seqs)} of {wl.num_seqs} sequences ({tok} tokens, all "
                          f"{wl.n_q_heads} query heads){' of the first step' if multi else ''}"
                          f" x {reps_cpu} repetitions, {cdt:.1f} s, single thread"}
+        # the same sample with the attention rows spread over every host core
+        ncores = os.cpu_count() or 1
+        if ncores > 1:
+            c0 = time.perf_counter()
+            reps_all, nbytes = 0, 0
+            while True:
+                nbytes += cpu_oracle_step(sub["wl"], sub["vals"], sub["seqs"], fp8,
+                                          threads=ncores)
+                reps_all += 1
+                if time.perf_counter() - c0 > 5.0 or reps_all >= 1000:
+                    break
+            adt = time.perf_counter() - c0
+            cpu["all_cores"] = {"value": nbytes / adt / 1e9, "unit": "GB/s", "cores": ncores,
+                                "sample": f"the same sample x {reps_all} repetitions, "
+                                          f"{adt:.1f} s, attention rows over {ncores} threads"}
 
     unique = None
     if multi:
