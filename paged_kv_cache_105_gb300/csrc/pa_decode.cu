@@ -1257,36 +1257,113 @@ struct MergeArgs {
   const int32_t* seq_lens;
   const int4* pair_info;
   int num_seqs, n_q, n_kv, group, part_tokens, max_parts, len_cap, balanced;
+  int coop;  // 1: one CTA per row, its warps sharing the row's parts (few rows)
 };
 
 constexpr int kMergeWarps = 8;
 
+// The parts of merge row `row`: part q lives in partial row
+// q == 0 ? rfirst : rbase + q * rstep. Returns their number (0 or 1: the
+// decode kernel wrote the output itself).
+__device__ __forceinline__ int merge_row_parts(const MergeArgs& m, int row, long long& rfirst,
+                                               long long& rbase, long long& rstep) {
+  const int s = row / m.n_q;
+  const int len = clamp_len(__ldg(&m.seq_lens[s]), m.len_cap);
+  if (m.balanced) {
+    // Balanced split: parts are warps c0 .. c0 + n - 1; warp c keeps slot
+    // (2c + slot) * G + head; only c0 may use slot 1.
+    const int h = row - s * m.n_q, g = h / m.group, n = h - g * m.group;
+    const int4 pi = __ldcg(&m.pair_info[(int64_t)s * m.n_kv + g]);
+    rfirst = ((long long)pi.x * 2 + pi.z) * m.group + n;
+    rbase = (long long)pi.x * 2 * m.group + n;
+    rstep = 2LL * m.group;
+    return len > 0 ? pi.y : 0;
+  }
+  rbase = rfirst = (long long)row * m.max_parts;
+  rstep = 1;
+  return parts_of(len, m.part_tokens);
+}
+
+// One row merged by a whole CTA (launched when there are few rows, e.g. one
+// long sequence whose pairs are cut into hundreds of parts): warp w folds
+// parts w, w + 8, ... into a running (max, sum, O), kB parts per round trip;
+// warp 0 then combines the eight with the same identity.
+template <int D>
+__device__ __forceinline__ void merge_row_coop(const MergeArgs& m, int row) {
+  constexpr int PER = D / 32, kB = 4;
+  __shared__ float s_acc[kMergeWarps][D];
+  __shared__ float2 s_ml[kMergeWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long rfirst, rbase, rstep;
+  const int nparts = merge_row_parts(m, row, rfirst, rbase, rstep);
+  if (nparts <= 1) return;  // the same on every thread of the CTA
+  auto rowq = [&](int q) -> long long { return q == 0 ? rfirst : rbase + q * rstep; };
+  float M = -INFINITY, L = 0.f, acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int q0 = warp; q0 < nparts; q0 += kMergeWarps * kB) {
+    float2 ml[kB];
+    float ov[kB][PER];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int q = q0 + b * kMergeWarps;
+      const bool in = q < nparts;
+      const long long r = rowq(in ? q : 0);
+      ml[b] = in ? __ldcg(&m.ws_ml[r]) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) ov[b][i] = in ? __ldcg(m.ws_o + r * D + lane + 32 * i) : 0.f;
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      if (ml[b].x == -INFINITY) continue;  // absent, or a part that saw only masked tokens
+      const float mx = fmaxf(M, ml[b].x);
+      const float sc = M == -INFINITY ? 0.f : fast_exp2(M - mx);
+      const float w = fast_exp2(ml[b].x - mx);
+      L = L * sc + w * ml[b].y;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = acc[i] * sc + w * ov[b][i];
+      M = mx;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) s_acc[warp][lane + 32 * i] = acc[i];
+  if (lane == 0) s_ml[warp] = make_float2(M, L);
+  __syncthreads();
+  if (warp != 0) return;
+  float Mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Mx = fmaxf(Mx, s_ml[w].x);
+  float Lt = 0.f, out[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) out[i] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    const float2 v = s_ml[w];
+    const float wt = v.x == -INFINITY ? 0.f : fast_exp2(v.x - Mx);
+    Lt += wt * v.y;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) out[i] += wt * s_acc[w][lane + 32 * i];
+  }
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    m.out[(int64_t)row * D + lane + 32 * i] = __float2bfloat16_rn(out[i] * inv);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs m) {
   griddep_wait();  // the partials come from the decode grid
+  if (m.coop) {  // grid = rows
+    merge_row_coop<D>(m, blockIdx.x);
+    return;
+  }
   constexpr int PER = D / 32;
   const int lane = threadIdx.x & 31;
   const int rows = m.num_seqs * m.n_q;
   for (int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5); row < rows;
        row += gridDim.x * kMergeWarps) {
-    const int s = row / m.n_q;
-    const int len = clamp_len(__ldg(&m.seq_lens[s]), m.len_cap);
-    int nparts;
     long long rbase, rfirst, rstep;  // row of part q: q == 0 ? rfirst : rbase + q * rstep
-    if (m.balanced) {
-      // Balanced split: parts are warps c0 .. c0 + n - 1; warp c keeps slot
-      // (2c + slot) * G + head; only c0 may use slot 1.
-      const int h = row - s * m.n_q, g = h / m.group, n = h - g * m.group;
-      const int4 pi = __ldcg(&m.pair_info[(int64_t)s * m.n_kv + g]);
-      nparts = len > 0 ? pi.y : 0;
-      rfirst = ((long long)pi.x * 2 + pi.z) * m.group + n;
-      rbase = (long long)pi.x * 2 * m.group + n;
-      rstep = 2LL * m.group;
-    } else {
-      nparts = parts_of(len, m.part_tokens);
-      rbase = rfirst = (long long)row * m.max_parts;
-      rstep = 1;
-    }
+    const int nparts = merge_row_parts(m, row, rfirst, rbase, rstep);
     if (nparts <= 1) continue;  // written directly by the decode kernel
     auto rowq = [&](int q) -> long long { return q == 0 ? rfirst : rbase + q * rstep; };
     // One round trip for the statistics (lane q holds part q) and the first
@@ -1534,9 +1611,12 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
     m.max_parts = a.max_parts;
     m.len_cap = a.len_cap;
     const int64_t rows = (int64_t)a.num_seqs * a.n_q;
-    int64_t mgrid = (rows + kMergeWarps - 1) / kMergeWarps;
+    // Few rows (up to two per SM): a CTA per row, so that a row cut into many
+    // parts is merged by eight warps; otherwise a warp per row.
+    m.coop = rows <= 2LL * num_sms();
+    int64_t mgrid = m.coop ? rows : (rows + kMergeWarps - 1) / kMergeWarps;
     const int64_t mcap = (int64_t)num_sms() * 8;
-    if (mgrid > mcap) mgrid = mcap;
+    if (!m.coop && mgrid > mcap) mgrid = mcap;
     cudaLaunchConfig_t mc = {};
     mc.gridDim = dim3((unsigned)mgrid);
     mc.blockDim = dim3(kMergeWarps * 32);
