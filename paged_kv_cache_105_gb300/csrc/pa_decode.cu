@@ -1261,6 +1261,9 @@ struct MergeArgs {
 };
 
 constexpr int kMergeWarps = 8;
+#ifndef PA_COOP_ROWS_PER_SM
+#define PA_COOP_ROWS_PER_SM 2  // a CTA per merge row up to this many rows per SM
+#endif
 
 // The parts of merge row `row`: part q lives in partial row
 // q == 0 ? rfirst : rbase + q * rstep. Returns their number (0 or 1: the
@@ -1613,7 +1616,7 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
     const int64_t rows = (int64_t)a.num_seqs * a.n_q;
     // Few rows (up to two per SM): a CTA per row, so that a row cut into many
     // parts is merged by eight warps; otherwise a warp per row.
-    m.coop = rows <= 2LL * num_sms();
+    m.coop = rows <= (long long)PA_COOP_ROWS_PER_SM * num_sms();
     int64_t mgrid = m.coop ? rows : (rows + kMergeWarps - 1) / kMergeWarps;
     const int64_t mcap = (int64_t)num_sms() * 8;
     if (!m.coop && mgrid > mcap) mgrid = mcap;
