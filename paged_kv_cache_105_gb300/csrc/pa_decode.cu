@@ -61,7 +61,10 @@ constexpr int kMaxParts = 1024;
 constexpr int kMaxSeqs = 8192;
 constexpr int kMaxGrid = 512;                       // persistent CTAs at most
 constexpr int kMaxWorkers = kMaxGrid * 4;           // balanced split: one worker per warp
-constexpr int kMinUnitsPerWorker = 8;               // balanced split: work per warp at least
+#ifndef PA_MIN_UNITS_PER_WORKER
+#define PA_MIN_UNITS_PER_WORKER 8
+#endif
+constexpr int kMinUnitsPerWorker = PA_MIN_UNITS_PER_WORKER;  // balanced split: work per warp at least
 #ifndef PA_PAIR_COST
 #define PA_PAIR_COST 4
 #endif
