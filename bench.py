@@ -37,6 +37,10 @@ METRIC = "paged decode attention: KV-read HBM GB/s (% of peak), tokens attended/
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 KERNEL_SOURCES = ["paged_kv_cache_105_gb300/csrc/pa_decode.cu",
                   "paged_kv_cache_105_gb300/csrc/pa_ptx.cuh"]
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_traffic.txt")
+PREFILL_SOURCES = ["paged_kv_cache_105_gb300/csrc/pa_prefill.cu",
+                   "paged_kv_cache_105_gb300/csrc/pa_tc.cuh",
+                   "paged_kv_cache_105_gb300/csrc/pa_ptx.cuh"]
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -108,27 +112,27 @@ def whole_job_rate(units_per_rank, world, seconds):
     return world * units_per_rank / seconds
 
 
-def kernel_hash():
+def kernel_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload_name):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on this workload with the current kernel source."""
-    if not os.path.exists(TRAFFIC_FILE):
+def recorded_traffic(workload_name, path=TRAFFIC_FILE, sources=KERNEL_SOURCES):
+    """DRAM bytes per launch from a committed ncu summary (decode by default),
+    if it was taken on this workload with the current kernel source."""
+    if not os.path.exists(path):
         return None
     kv = {}
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
     key = f"traffic_bytes_per_launch[{workload_name}]"
-    if kv.get("kernel_source_sha256") != kernel_hash() or key not in kv:
+    if kv.get("kernel_source_sha256") != kernel_hash(sources) or key not in kv:
         return None
     return float(kv[key])
 
@@ -507,7 +511,9 @@ def run_prefill(args):
                                      "product runs twice",
                        "launch": "one CUDA graph replay per step (write, prefill)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(wl.name, PREFILL_TRAFFIC_FILE,
+                                                     PREFILL_SOURCES),
                          "kernel": "prefill_tc_kernel (pa_prefill)",
                          "peak_source": f"{kind} bf16_tflops (cuBLAS, burst)",
                          "prefill_ms_avg": att_ms},
