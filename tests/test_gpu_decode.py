@@ -170,6 +170,21 @@ def test_balanced_split_pair_cut_into_many_pieces(hq, hkv, d):
     assert a < 1e-2 and r < 2e-2
 
 
+@pytest.mark.parametrize("extra", [0, 1])
+@pytest.mark.parametrize("P", [0, 256])
+def test_merge_on_both_sides_of_the_cta_per_row_switch(extra, P):
+    # the merge takes a CTA per row up to two rows per SM and a warp per row
+    # beyond: rows = sequences here (one query head), at the switch and one past
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    n = 2 * sms + extra
+    rng = np.random.default_rng(n + P)
+    lens = rng.integers(1, 200, size=n).tolist()
+    lens[n // 2] = 9000  # a pair cut into many parts
+    wl = W.custom(lens, block_size=16, n_q_heads=1, n_kv_heads=1, head_dim=64, seed=n)
+    (a, r), _, _ = full_parity(wl, partition_tokens=P)
+    assert a < 1e-2 and r < 2e-2
+
+
 def test_block_placement_does_not_matter():
     base = W.custom([900, 33, 1500], block_size=16, n_q_heads=8, n_kv_heads=8, head_dim=128,
                     seed=21)
