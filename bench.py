@@ -112,11 +112,20 @@ def whole_job_rate(units_per_rank, world, seconds):
     return world * units_per_rank / seconds
 
 
+def _code_tokens(text):
+    """C/CUDA source without its comments and blank space: what the compiler
+    sees, so that a comment edit does not invalidate a recorded capture."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
     for f in sources:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_tokens(fh.read()).encode())
     return h.hexdigest()
 
 

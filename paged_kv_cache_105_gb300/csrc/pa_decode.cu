@@ -7,32 +7,39 @@
 // sequence's block table. The pages describe no kernel design; everything
 // below is this library's.
 //
-// Design (one GPU, HBM-bound: every step reads all cached K/V once):
-//  * Work items are (sequence, kv head, partition of P tokens), numbered
-//    sequence-major from per-sequence prefix sums that every CTA builds in
-//    shared memory. Persistent CTAs (two per SM) take items from a global
-//    counter; a CTA learns its next-but-one item while it works on the
-//    current one, through a small shared-memory mailbox.
-//  * A CTA has 4 warps. An item's 16-token units are dealt round-robin to
-//    them and every warp streams its own units: lane 0 issues TMA tile loads
-//    (128-byte swizzle) of the unit's K and V rows into the warp's stage
-//    ring, one mbarrier per stage. Each warp keeps its ring full across item
-//    boundaries: the next item's table entries, query fragments and first
-//    units are already in flight while the CTA merges the current item.
-//  * The GQA group (the G query heads sharing the kv head) is the N side of
-//    bf16 mma.sync m16n8k16 with the tokens on M: S^T = K Q^T, then
+// Design (one GPU, HBM-bound: every step reads all cached K/V once). The
+// unit of streaming is 16 tokens of one (sequence, kv head): one 16-token
+// block, two 8-token blocks or half a 32-token block. Two kernels split the
+// work; both end in the same merge.
+//  * Balanced split (split_kernel, the default): the (sequence, kv head)
+//    pairs, in order, form one stream of units (plus a small cost per pair),
+//    cut into equal contiguous shares, one per warp of a persistent grid (3
+//    CTAs of 4 warps per SM). A warp walks its share in chunks of up to 32
+//    units through its own stage ring (lane 0 issues the TMA tile loads,
+//    128-byte swizzle, one mbarrier per stage) with no barrier and no
+//    cross-warp exchange; the ring runs across chunk and pair boundaries. A
+//    pair wholly inside a share is written straight from the warp's
+//    registers; a cut pair leaves a partial in one of the warp's two slots.
+//  * Fixed partitions (decode_kernel): items are (sequence, kv head,
+//    partition of P tokens), numbered sequence-major from per-sequence prefix
+//    sums that every CTA builds in shared memory. Persistent CTAs take items
+//    from a global counter and learn their next-but-one item through a
+//    shared-memory mailbox while they work; an item's units are dealt
+//    round-robin to the CTA's 4 warps, whose states meet in shared memory in
+//    two rounds (warps 2, 3 -> 0, 1, then 1 -> 0).
+//  * Math: the GQA group (the G query heads sharing the kv head) is the N
+//    side of bf16 mma.sync m16n8k16 with the tokens on M: S^T = K Q^T, then
 //    O^T += V^T P^T; movmatrix turns the score fragment into the P^T operand
 //    in registers. Online softmax in fp32, base 2; the running maximum is
-//    moved (and the state rescaled) only when a score exceeds it by 2^8.
-//  * Warps 1-3 hand their state to warp 0 through shared memory; a
-//    one-partition sequence writes its bf16 output directly, otherwise the
-//    partition's (O, m, l) goes to the workspace and a second, small kernel
-//    (one warp per query row) merges the partitions with log-sum-exp
-//    weights. It is a programmatic dependent launch: it starts while the
-//    decode grid drains and waits on the grid dependency before reading.
+//    moved (and the state rescaled) only when a score exceeds it by 2^8. The
+//    fp8 variant converts E4M3 codes to f16 in registers after the byte load.
+//  * Merge: a second, small kernel combines the partials with log-sum-exp
+//    weights (a warp per query row, or a CTA per row when rows are few). It
+//    is a programmatic dependent launch that waits on the grid dependency
+//    before reading.
 //  * The decode grid itself is a programmatic dependent of whatever precedes
 //    it on the stream (normally the cache write), so its launch overlaps that
-//    kernel; it waits on the dependency before reading any input.
+//    kernel; it waits on the dependency before reading the pools.
 //  * Every mbarrier wait is bounded; on timeout the kernel flags
 //    PA_DEV_ERR_TIMEOUT and keeps its control flow, so it always terminates.
 #include <cuda.h>
@@ -69,7 +76,7 @@ constexpr int kMinUnitsPerWorker = PA_MIN_UNITS_PER_WORKER;  // balanced split: 
 #define PA_PAIR_COST 4
 #endif
 // Balanced split: each (sequence, kv head) pair also costs this many units in
-// the stream being cut (its merge and bookkeeping), so a CTA whose share holds
+// the stream being cut (its merge and bookkeeping), so a warp whose share holds
 // many short pairs gets fewer units.
 constexpr int kPairCost = PA_PAIR_COST;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -89,7 +96,7 @@ struct DecodeArgs {
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
   int part_tokens, max_parts, len_cap;
-  int balanced;              // 1: even split of all units across CTAs
+  int balanced;              // 1: even split of all units across warps
   int map3d;                 // 1: one TMA op loads both 64-column halves of a row
   float scale_log2;          // softmax scale (times the K scale for fp8) times log2(e)
   float v_scale;             // fp8: the V scale; 1 for bf16
@@ -204,8 +211,8 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, cons
 
 // A chunk of work: up to 128 units of one (sequence, kv head). `part` says
 // where the result goes (-1: the output itself; fixed partitions: the
-// partition index; balanced split: this CTA's partial slot 0 or 1). A
-// segment (one CTA's share of one (sequence, kv head)) may span several
+// partition index; balanced split: this warp's partial slot 0 or 1). A
+// segment (one warp's share of one (sequence, kv head)) may span several
 // chunks: the softmax state is reset at `first` and written at `last`.
 struct Item {
   int s, g, tok_end, u_begin, n_units, part;
@@ -241,10 +248,10 @@ __device__ __forceinline__ Item decode_item(int item, const int* prefix, const i
 
 // Balanced split: the (sequence, kv head) pairs in order (sequence-major)
 // form one stream; pair (s, g) occupies [A, B) = kPairCost positions of
-// bookkeeping then its 16-token units [A + kPairCost, B). CTA c owns
+// bookkeeping then its 16-token units [A + kPairCost, B). Warp c owns
 // positions [c W / n, (c+1) W / n) of the W-long stream. The chunk that
-// starts at or after position `pos` inside the CTA range [lo, hi): up to 128
-// units of one pair. Returns false if the range holds no more units.
+// starts at or after position `pos` inside the warp's range [lo, hi): up to
+// max_units units of one pair. Returns false if the range holds no more units.
 __device__ __forceinline__ bool decode_chunk(long long pos, long long lo, long long hi,
                                              const int* prefix, const int* lens,
                                              const DecodeArgs& a, Item& it,
