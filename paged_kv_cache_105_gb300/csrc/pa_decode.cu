@@ -950,6 +950,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   }
 }
 
+#ifndef PA_SPLIT_BUDGET_FP8
+#define PA_SPLIT_BUDGET_FP8 8192  // stage-ring bytes per warp, E4M3 cache: 2 stages
+#endif
 #ifndef PA_SPLIT_BUDGET
 #define PA_SPLIT_BUDGET 16384
 #endif
@@ -960,7 +963,7 @@ template <int D, int BS, int NT, bool FP8 = false>
 struct SplitCfg {
   using C = Cfg<D, BS, NT, FP8 ? 1 : 2>;
   static constexpr int STAGE = C::STAGE;
-  static constexpr int STAGES_RAW = PA_SPLIT_BUDGET / STAGE;
+  static constexpr int STAGES_RAW = (FP8 ? PA_SPLIT_BUDGET_FP8 : PA_SPLIT_BUDGET) / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
   static constexpr int MISC_OFF = BAR_OFF + kWarps * STAGES * 8;
