@@ -1274,6 +1274,9 @@ struct MergeArgs {
 };
 
 constexpr int kMergeWarps = 8;
+#ifndef PA_MERGE_PRE
+#define PA_MERGE_PRE 8  // parts a merge warp reads with the statistics, then per round
+#endif
 #ifndef PA_COOP_ROWS_PER_SM
 #define PA_COOP_ROWS_PER_SM 2  // a CTA per merge row up to this many rows per SM
 #endif
@@ -1383,8 +1386,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
     if (nparts <= 1) continue;  // written directly by the decode kernel
     auto rowq = [&](int q) -> long long { return q == 0 ? rfirst : rbase + q * rstep; };
     // One round trip for the statistics (lane q holds part q) and the first
-    // kPre parts' rows; the rest stream in pairs.
-    constexpr int kPre = 4;
+    // kPre parts' rows; the rest stream kPre at a time.
+    constexpr int kPre = PA_MERGE_PRE;
     float2 st = make_float2(-INFINITY, 0.f);
     if (lane < nparts) st = __ldcg(&m.ws_ml[rowq(lane)]);
     float pre[kPre][PER];
