@@ -157,6 +157,37 @@ extern "C" int paref_alloc_free_seq(paref_alloc* a, int seq) {
   return returned;
 }
 
+// Usage of the live pool ("03 · PagedAttention", Try It: stored tokens over
+// allocated slots; "PagedAttention" (mlapandio.dev), closing advice: watch the
+// share of the pool in use). A block in use holds as many tokens as the
+// furthest any sequence mapping it has written into it; sharers of a block
+// hold the same tokens there, since a write into a shared block copies it
+// first, so a shared block counts once.
+extern "C" void paref_alloc_usage(const paref_alloc* a, int64_t* tokens, int64_t* slots,
+                                  int64_t* blocks_in_use) {
+  const int bs = a->block_size;
+  std::vector<int> fill(a->refcount.size(), 0);
+  for (size_t s = 0; s < a->tables.size(); ++s) {
+    if (!a->alive[s]) continue;
+    const std::vector<int32_t>& t = a->tables[s];
+    for (size_t j = 0; j < t.size(); ++j) {
+      int64_t in_block = (int64_t)a->lens[s] - (int64_t)j * bs;
+      int n = in_block >= bs ? bs : (int)in_block;
+      if (n > fill[t[j]]) fill[t[j]] = n;
+    }
+  }
+  int64_t tok = 0, used = 0;
+  for (size_t b = 0; b < a->refcount.size(); ++b) {
+    if (a->refcount[b] > 0) {
+      ++used;
+      tok += fill[b];
+    }
+  }
+  if (tokens) *tokens = tok;
+  if (slots) *slots = used * bs;
+  if (blocks_in_use) *blocks_in_use = used;
+}
+
 extern "C" int paref_alloc_num_free(const paref_alloc* a) { return (int)a->free_stack.size(); }
 extern "C" int paref_alloc_num_blocks(const paref_alloc* a) { return (int)a->refcount.size(); }
 

@@ -72,6 +72,12 @@ int paref_alloc_fork(paref_alloc* a, int seq);
    Returns the number of blocks returned to the free list. */
 int paref_alloc_free_seq(paref_alloc* a, int seq);
 
+/* Usage of the live pool: *tokens = tokens held, a block in use counting
+   the furthest any sequence mapping it has written into it (a shared block
+   counts once); *slots = blocks in use * block_size; *blocks_in_use = blocks
+   with refcount > 0. Any output pointer may be NULL. */
+void paref_alloc_usage(const paref_alloc* a, int64_t* tokens, int64_t* slots,
+                       int64_t* blocks_in_use);
 int paref_alloc_num_free(const paref_alloc* a);
 int paref_alloc_num_blocks(const paref_alloc* a);
 int paref_alloc_refcount(const paref_alloc* a, int block);

@@ -41,6 +41,8 @@ def lib():
                 "paref_alloc_fork": (C.c_int, [C.c_void_p, C.c_int]),
                 "paref_alloc_free_seq": (C.c_int, [C.c_void_p, C.c_int]),
                 "paref_alloc_num_free": (C.c_int, [C.c_void_p]),
+                "paref_alloc_usage": (None, [C.c_void_p, C.POINTER(C.c_int64),
+                                             C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
                 "paref_alloc_num_blocks": (C.c_int, [C.c_void_p]),
                 "paref_alloc_refcount": (C.c_int, [C.c_void_p, C.c_int]),
                 "paref_alloc_seq_len": (C.c_int, [C.c_void_p, C.c_int]),
@@ -177,6 +179,25 @@ class Allocator:
         if r < 0:
             raise ValueError(f"bad sequence id {seq}")
         return r
+
+    def usage(self):
+        """(tokens held, slots of the blocks in use, blocks in use); a shared
+        block counts once, holding what its furthest writer put there."""
+        t, s, b = C.c_int64(), C.c_int64(), C.c_int64()
+        lib().paref_alloc_usage(self._h, C.byref(t), C.byref(s), C.byref(b))
+        return t.value, s.value, b.value
+
+    def utilisation(self) -> float:
+        """Tokens held / slots allocated ("03 · PagedAttention", Try It: the
+        utilisation column); 0.0 for an empty pool."""
+        t, s, _ = self.usage()
+        return t / s if s else 0.0
+
+    def cache_usage(self) -> float:
+        """Blocks in use / pool blocks (the share of the KV pool taken, the
+        figure the mlapandio page's closing advice says to watch)."""
+        _, _, b = self.usage()
+        return b / self.num_blocks if self.num_blocks else 0.0
 
     @property
     def num_free(self) -> int:

@@ -103,3 +103,56 @@ def test_capacity_is_floor():
     assert paref.capacity(100, 10, 1) == 10
     assert paref.capacity(99, 10, 1) == 9
     assert paref.capacity(100, 0, 1) == 0
+
+
+def _grow(alloc, lens):
+    """Sequences of the given lengths, grown one token at a time."""
+    seqs = [alloc.add_seq() for _ in lens]
+    for s, L in zip(seqs, lens):
+        for _ in range(L):
+            alloc.append(s)
+    return seqs
+
+
+def test_allocator_utilisation_fragmentation(golden):
+    # The Try It experiment grown through the allocator itself: the live pool
+    # holds the experiment's stored tokens in its paged slots (98.0% at bs 16).
+    g = golden("fragmentation.json")
+    lens = _fragmentation_lengths(g["N"], g["max_len"])
+    pool = g["paged_alloc_bs16"] // 16 + 100
+    alloc = paref.Allocator(pool, 16)
+    _grow(alloc, lens)
+    tokens, slots, blocks = alloc.usage()
+    assert tokens == g["tokens_stored"]
+    assert slots == g["paged_alloc_bs16"]
+    assert blocks == g["paged_alloc_bs16"] // 16
+    assert pct1(alloc.utilisation()) == g["paged_util_pct_1dp_bs16"]
+    assert alloc.cache_usage() == blocks / pool
+
+
+def test_allocator_utilisation_worked_example(golden):
+    g = golden("worked_example.json")
+    alloc = paref.Allocator(256, g["page"])
+    _grow(alloc, g["lengths"])
+    assert alloc.usage() == (g["used_tokens"], g["paged_alloc_total"],
+                             g["paged_alloc_total"] // g["page"])
+    assert alloc.utilisation() == g["used_tokens"] / g["paged_alloc_total"]
+    assert pct1(1 - alloc.utilisation()) == g["paged_waste_pct_1dp"]
+
+
+def test_allocator_utilisation_counts_a_shared_block_once():
+    # 20 tokens at bs 16: blocks of 16 and 4 tokens. A fork shares both; its
+    # next token lands in the shared partial block, which is copied first.
+    alloc = paref.Allocator(8, 16)
+    (s,) = _grow(alloc, [20])
+    assert alloc.usage() == (20, 32, 2)
+    f = alloc.fork(s)
+    assert alloc.usage() == (20, 32, 2)                  # nothing new held
+    _, pair = alloc.append(f)
+    assert pair is not None
+    assert alloc.usage() == (16 + 4 + 5, 48, 3)          # the copy holds 5 tokens
+    alloc.free(s)                                        # its partial block goes back
+    assert alloc.usage() == (16 + 5, 32, 2)
+    alloc.free(f)
+    assert alloc.usage() == (0, 0, 0)
+    assert alloc.utilisation() == 0.0 and alloc.cache_usage() == 0.0
