@@ -366,11 +366,14 @@ pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void
  * GPU that loads the library holds those 64 MiB until the process exits. It
  * calls no allocator (no cudaMalloc, cudaFree or allocating library routine).
  *
- *  - The first call on a device looks the array's device address up (one
- *    cudaGetSymbolAddress with that device current). Make that first call
- *    before any stream capture.
- *  - Each call first clears the scratch's counters on `stream` (an
- *    asynchronous memset), then runs the decode on `stream`.
+ *  - The first call from a CUDA context (normally the device's primary
+ *    context) looks the array's device address up: one cudaGetSymbolAddress
+ *    with that context current, cached under the context's id. A context
+ *    made after a device reset, or one the caller created, gets its own
+ *    lookup. Make the first call on each device before any stream capture.
+ *  - Each call checks every argument first; a refused call launches
+ *    nothing. Then it clears the scratch's counters on `stream` (an
+ *    asynchronous memset) and runs the decode on `stream`.
  *  - All calls in the process share the one array. Calls that may overlap on
  *    the GPU (different streams without ordering, or several host threads)
  *    race on it and give wrong results; order them on one stream.

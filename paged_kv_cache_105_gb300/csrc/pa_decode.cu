@@ -348,14 +348,34 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Item
 // exactly as well as weights below 1. (m, l) keep their meaning: l is the sum
 // of 2^(x - m) and O the matching weighted sum, whatever m is. sc holds the
 // raw scores of tokens tA = g (sc[..][0..1]) and tB = g + 8 (sc[..][2..3]);
-// masked tokens weigh zero. P^T fragments come back in pb (f16 or bf16).
+// masked tokens weigh zero. P^T fragments come back in pb (f16 or bf16) as a
+// pair: pb[..][0..1] the rounded weights, pb[..][2..3] what rounding left
+// (split_pair); both go through the P V product.
 constexpr float kLazyLog2 = 8.f;
+
+// Two weights as a 16-bit pair hi + lo: hi = p rounded to the operand type,
+// lo = (p - hi) rounded, so hi + lo carries p to about 2^-16 relative. A lone
+// 16-bit weight is off by up to 2^-8 (bf16) or 2^-11 (f16) relative, which
+// is too coarse for an output element that is a near-cancelling sum of
+// larger terms (short contexts): there the error of the weights, not of the
+// element, sets the element's error. p - hi is exact in fp32.
+template <bool F16P>
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  if constexpr (F16P) {
+    hi = pack_f16x2(p0, p1);
+    const float2 h = unpack_f16x2(hi);
+    lo = pack_f16x2(p0 - h.x, p1 - h.y);
+  } else {
+    hi = pack_bf16x2(p0, p1);
+    lo = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+  }
+}
 
 template <int NT, int KS, bool F16P>
 __device__ __forceinline__ void softmax_unit(const float (&sc)[NT][4], bool okA, bool okB,
                                              float scale_log2, float (&acc)[NT][KS][4],
                                              float (&mrun)[NT][2], float (&lrun)[NT][2],
-                                             uint32_t (&pb)[NT][2]) {
+                                             uint32_t (&pb)[NT][4]) {
   float x[NT][4];
   bool need = false;
 #pragma unroll
@@ -395,13 +415,13 @@ __device__ __forceinline__ void softmax_unit(const float (&sc)[NT][4], bool okA,
       pv[jj + 2] = fast_exp2(x[t][jj + 2] - base);
       lrun[t][jj] += pv[jj] + pv[jj + 2];
     }
-    if constexpr (F16P) {
-      pb[t][0] = movmatrix_trans(pack_f16x2(pv[0], pv[1]));
-      pb[t][1] = movmatrix_trans(pack_f16x2(pv[2], pv[3]));
-    } else {
-      pb[t][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
-      pb[t][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
-    }
+    uint32_t hA, lA, hB, lB;
+    split_pair<F16P>(pv[0], pv[1], hA, lA);
+    split_pair<F16P>(pv[2], pv[3], hB, lB);
+    pb[t][0] = movmatrix_trans(hA);
+    pb[t][1] = movmatrix_trans(hB);
+    pb[t][2] = movmatrix_trans(lA);
+    pb[t][3] = movmatrix_trans(lB);
   }
 }
 
@@ -441,7 +461,7 @@ __device__ __forceinline__ void attend_unit(uint32_t kb, uint32_t vb, int lane, 
     const int tA = lane >> 2, tB = tA + 8;
     const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
     const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
-    uint32_t pb[NT][2];
+    uint32_t pb[NT][4];
     softmax_unit<NT, KS, false>(sc, okA, okB, scale_log2, acc, mrun, lrun, pb);
     // ---- O^T += V^T P^T
     {
@@ -455,8 +475,10 @@ __device__ __forceinline__ void attend_unit(uint32_t kb, uint32_t vb, int lane, 
         uint32_t a0, a1, a2, a3;
         ldsm_x4_trans(row + h * ROWS * 128 + ((c ^ (r & 7)) << 4), a0, a1, a2, a3);
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
+        for (int t = 0; t < NT; ++t) {
           mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+          mma_bf16_16816(acc[t][dt], a0, a1, a2, a3, pb[t][2], pb[t][3]);
+        }
       }
     }
 }
@@ -542,7 +564,7 @@ __device__ __forceinline__ void attend_unit_fp8(uint32_t kb, uint32_t vb, int la
   const int tA = lane >> 2, tB = tA + 8;
   const bool okA = tA < nv && (mask >> (tA / ROWS) & 1);
   const bool okB = tB < nv && (mask >> (tB / ROWS) & 1);
-  uint32_t pb[NT][2];
+  uint32_t pb[NT][4];
   softmax_unit<NT, KS, true>(sc, okA, okB, scale_log2, acc, mrun, lrun, pb);
   // ---- O^T += V^T P^T
 #pragma unroll
@@ -558,8 +580,10 @@ __device__ __forceinline__ void attend_unit_fp8(uint32_t kb, uint32_t vb, int la
       const uint32_t a0 = movmatrix_trans(m1a), a1 = movmatrix_trans(m2a);
       const uint32_t a2 = movmatrix_trans(m1b), a3 = movmatrix_trans(m2b);
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
+      for (int t = 0; t < NT; ++t) {
         mma_f16_16816(acc[t][2 * p + hf], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+        mma_f16_16816(acc[t][2 * p + hf], a0, a1, a2, a3, pb[t][2], pb[t][3]);
+      }
     }
   }
 }
@@ -1750,7 +1774,8 @@ static pa_status decode_common(void* out, const void* q, const void* k_pool, con
                                int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                                float scale, int partition_tokens, int max_seq_len,
                                void* workspace, size_t workspace_bytes, int32_t* err_word,
-                               pa_stream_t stream, bool fp8, float k_scale, float v_scale) {
+                               pa_stream_t stream, bool fp8, float k_scale, float v_scale,
+                               bool clear_counters = false) {
   if (fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (fp8 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
     return PA_ERR_INVALID_ARG;
@@ -1775,6 +1800,15 @@ static pa_status decode_common(void* out, const void* q, const void* k_pool, con
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PA_ERR_INVALID_ARG;
   if (workspace_bytes < w.total) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (clear_counters) {
+    // A workspace shared with earlier calls: its work counters and pair
+    // descriptors must start at zero. Every check above has passed, so a
+    // call that is refused launches nothing.
+    cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.work_off, 0,
+                                    w.total - w.work_off, st);
+    if (e != cudaSuccess) return cuda_fail("pa_decode_noalloc memset", e);
+  }
 
   DecodeArgs a;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1801,7 +1835,6 @@ static pa_status decode_common(void* out, const void* q, const void* k_pool, con
   a.v_scale = fp8 ? v_scale : 1.f;
   a.map3d = 0;
   const int64_t items_upper = (int64_t)num_seqs * n_kv_heads * (w.max_parts > 0 ? w.max_parts : 1);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (fp8) return dispatch_bs<128, true>(block_size, a, k_pool, v_pool, items_upper, st);
   if (head_dim == 64) return dispatch_bs<64>(block_size, a, k_pool, v_pool, items_upper, st);
   return dispatch_bs<128>(block_size, a, k_pool, v_pool, items_upper, st);
@@ -1846,32 +1879,60 @@ namespace pa {
 // looked up once per device below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device (looked up on the
-// first call per device, with that device current). nullptr on failure.
+// Device address of g_noalloc_scratch in the calling thread's current
+// context. The address belongs to a context, not to a device index: it is
+// looked up (cudaGetSymbolAddress, with that context current) on the first
+// call from each context and cached under the context's process-unique id,
+// so that a context made after a device reset, or one the caller created
+// itself, gets its own lookup instead of a stale address. nullptr on failure.
 static void* noalloc_scratch(pa_status* st) {
   static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    *st = cuda_fail("pa_decode_noalloc cudaGetDevice", e);
-    return nullptr;
-  }
-  if (dev < 0 || dev >= 64) {
-    *st = cuda_fail_msg("pa_decode_noalloc", "device index above 63");
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  static PFN_cuCtxGetCurrent_v4000 get_ctx = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      *st = cuda_fail("pa_decode_noalloc cudaGetSymbolAddress", e);
-      return nullptr;
-    }
-    addr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_ctx || !get_id) {
+    *st = cuda_fail_msg("pa_decode_noalloc", "context queries unavailable");
+    return nullptr;
   }
-  return addr[dev];
+  // The context the kernel will run in. Without a current context the
+  // runtime makes the device's primary context current on its first call;
+  // the symbol lookup below is such a call, so look the context up after it.
+  auto current_id = [&](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+  };
+  constexpr int kSlots = 64;
+  static unsigned long long ids[kSlots];
+  static void* addrs[kSlots];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  unsigned long long id = 0;
+  if (current_id(&id))
+    for (int i = 0; i < used; ++i)
+      if (ids[i] == id) return addrs[i];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    *st = cuda_fail("pa_decode_noalloc cudaGetSymbolAddress", e);
+    return nullptr;
+  }
+  if (current_id(&id)) {  // cache it (the oldest entry gives way when full)
+    const int i = used < kSlots ? used++ : (next++ % kSlots);
+    ids[i] = id;
+    addrs[i] = p;
+  }
+  return p;
 }
 
 }  // namespace pa
@@ -1917,19 +1978,10 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_p
   pa_status st = PA_OK;
   void* scratch = noalloc_scratch(&st);
   if (scratch == nullptr) return st;
-  // The work counters must start at zero. A completed call leaves them
-  // zeroed, but the array is shared by every call in the process, so clear
-  // them here rather than trust the previous caller.
-  const int P = resolve_partition(num_seqs, n_kv_heads, block_size, max_seq_len,
-                                  partition_tokens);
-  WsLayout w;
-  if (P < 0 || !layout(num_seqs, n_q_heads, n_kv_heads, head_dim, P, max_seq_len, &w))
-    return PA_ERR_UNSUPPORTED;
-  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.work_off, 0,
-                                  w.total - w.work_off, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail("pa_decode_noalloc memset", e);
-  return pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
-                   max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim, block_size,
-                   scale, partition_tokens, max_seq_len, scratch, PA_NOALLOC_SCRATCH_BYTES,
-                   err_word, stream);
+  // The array is shared by every call in the process: its counters are
+  // cleared on `stream` once every argument check has passed.
+  return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                       max_blocks_per_seq, num_blocks, n_q_heads, n_kv_heads, head_dim,
+                       block_size, scale, partition_tokens, max_seq_len, scratch,
+                       PA_NOALLOC_SCRATCH_BYTES, err_word, stream, false, 1.f, 1.f, true);
 }

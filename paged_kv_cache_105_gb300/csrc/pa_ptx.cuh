@@ -149,6 +149,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return d;
 }
 
+// The two halves of an f16x2 as floats (exact), the low half in .x.
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(v));
+  return make_float2(lo, hi);
+}
+
 // Four E4M3 codes (bytes 0..3 of x) to two f16x2: lo = (byte 0, byte 1),
 // hi = (byte 2, byte 3), the lower byte in the lower half. Every E4M3 value
 // is exact in f16.

@@ -10,7 +10,14 @@ from paged_kv_cache_105_gb300 import binding as B
 from paged_kv_cache_105_gb300 import workloads as W
 
 ATOL = 1e-2       # max abs error, bf16 output vs fp64 oracle
-ROW_RTOL = 2e-2   # max over (seq, head) rows of ||gpu - ref||_2 / ||ref||_2
+RTOL = 2e-2       # max element-wise relative error |gpu - ref| / max(|ref|, REL_FLOOR)
+REL_FLOOR = 1e-2  # denominator floor: outputs are means of N(0, 1) values and can sit at 0
+ROW_RTOL = 2e-2   # also: max over (seq, head) rows of ||gpu - ref||_2 / ||ref||_2
+
+# Every compare() call appends (what, elements, max abs, max rel, max row rel,
+# the reference value at the worst relative element); the session prints the
+# maxima per workload at its end (tests/conftest.py).
+PARITY_REPORT: list = []
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -109,27 +116,67 @@ def sampled_oracle(wl: W.Workload, vals_dev: dict, seqs, fp8_scales=None):
     if fp8_scales is None:
         paref.copy_blocks(kp, vp, pairs)
         paref.reshape_and_cache(kn, vn, kp, vp, slots)
-        return paref.attention_paged(q, kp, vp, bt, lens, wl.scale)
+        return attention_threaded(paref.attention_paged, (q, kp, vp, bt, lens, wl.scale),
+                                  len(seqs), wl.n_q_heads, wl.head_dim)
     ks, vs = fp8_scales
     paref.copy_blocks(kp.view(np.uint16), vp.view(np.uint16), pairs)  # a byte copy
     paref.reshape_and_cache_fp8(kn, vn, kp, vp, slots, ks, vs)
-    return paref.attention_paged_fp8(q, kp, vp, bt, lens, wl.scale, ks, vs)
+    return attention_threaded(paref.attention_paged_fp8, (q, kp, vp, bt, lens, wl.scale, ks, vs),
+                              len(seqs), wl.n_q_heads, wl.head_dim)
 
 
-def compare(gpu_out: torch.Tensor, ref: np.ndarray, what=""):
-    """bf16 GPU output vs fp64 oracle: elementwise abs and row-wise relative."""
+def attention_threaded(fn, args, num_seqs, n_q_heads, head_dim, threads=None):
+    """The oracle's attention `fn(*args, rows=...)` over every (sequence, head)
+    row, the rows split across host threads (each oracle call releases the
+    interpreter lock). Same result as one call: rows are independent."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    rows = np.array([(s, h) for s in range(num_seqs) for h in range(n_q_heads)], np.int32)
+    threads = threads or max(1, min(32, os.cpu_count() or 1))
+    chunks = [c for c in np.array_split(rows, threads) if len(c)]
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(lambda c: fn(*args, rows=c), chunks))
+    return np.concatenate(parts, 0).reshape(num_seqs, n_q_heads, head_dim)
+
+
+class Parity(tuple):
+    """(max_abs, max_rel) of one comparison, plus the row-wise figure."""
+
+    def __new__(cls, max_abs, max_rel, max_row_rel):
+        obj = super().__new__(cls, (max_abs, max_rel))
+        obj.max_abs, obj.max_rel, obj.max_row_rel = max_abs, max_rel, max_row_rel
+        return obj
+
+    def __str__(self):
+        return (f"max_abs={self.max_abs:.2e} max_rel={self.max_rel:.2e} "
+                f"max_row_rel={self.max_row_rel:.2e}")
+
+
+def compare(gpu_out: torch.Tensor, ref: np.ndarray, what="") -> Parity:
+    """bf16 GPU output vs fp64 oracle, element by element: |gpu - ref| <= ATOL
+    and |gpu - ref| / max(|ref|, REL_FLOOR) <= RTOL for every element. The
+    row-wise relative L2 error is computed and asserted as well."""
     g = gpu_out.detach().float().cpu().numpy().astype(np.float64)
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - ref)
     max_abs = float(err.max()) if err.size else 0.0
+    rel_el = err / np.maximum(np.abs(ref), REL_FLOOR)
+    worst = int(np.argmax(rel_el)) if rel_el.size else 0
+    max_rel = float(rel_el.flat[worst]) if rel_el.size else 0.0
     num = np.sqrt((err ** 2).sum(-1))
     den = np.sqrt((ref ** 2).sum(-1))
     rel = np.where(den > 0, num / np.maximum(den, 1e-30), num)
-    max_rel = float(rel.max()) if rel.size else 0.0
+    max_row = float(rel.max()) if rel.size else 0.0
+    PARITY_REPORT.append((what, int(err.size), max_abs, max_rel, max_row,
+                          float(ref.flat[worst]) if ref.size else 0.0))
+    where = np.unravel_index(worst, ref.shape) if ref.size else ()
     assert max_abs <= ATOL, f"{what}: max abs err {max_abs:.3e} > {ATOL}"
-    assert max_rel <= ROW_RTOL, f"{what}: max row rel err {max_rel:.3e} > {ROW_RTOL}"
-    return max_abs, max_rel
+    assert max_rel <= RTOL, (f"{what}: max element rel err {max_rel:.3e} > {RTOL} at "
+                             f"{tuple(int(i) for i in where)} (ref {ref.flat[worst]:.4e}, "
+                             f"gpu {g.flat[worst]:.4e})")
+    assert max_row <= ROW_RTOL, f"{what}: max row rel err {max_row:.3e} > {ROW_RTOL}"
+    return Parity(max_abs, max_rel, max_row)
 
 
 # ------------------------------------------------------------------ fp8 cache

@@ -1,9 +1,11 @@
 """GPU parity of paged decode attention against the fp64 oracle.
 
-Bar: every bf16 output within 1e-2 of the oracle, and every (sequence, head)
-row within 2e-2 relative L2 error. Small workloads are compared in full;
-the two large ones (the fragmented MHA sweep and the 32k-token split-KV
-batch) at their full sizes, on sampled sequences the oracle can afford."""
+Bar, element by element: |gpu - ref| <= 1e-2 and |gpu - ref| / max(|ref|,
+1e-2) <= 2e-2 for every bf16 output; every (sequence, head) row is also held
+to 2e-2 relative L2 error. Small workloads are compared in full; the two
+large ones at their full sizes: the 32k-token split-KV batch on all of its
+sequences, the fragmented MHA sweep on 36 of its 256 (the shortest, the
+longest and 32 drawn at random)."""
 import numpy as np
 import pytest
 import torch
@@ -51,9 +53,11 @@ def test_fragmented_mha_full_size_sampled(bs):
     wl = W.config3(block_size=bs)
     vals = W.make_values(wl, device=DEV, poison_tails=True)
     rng = np.random.default_rng(bs)
-    order = np.argsort(wl.seq_lens)
-    seqs = sorted(set([int(order[0]), int(order[-1])] +
-                      rng.choice(wl.num_seqs, 4, replace=False).tolist()))
+    order = np.argsort(wl.seq_lens, kind="stable")
+    # the two shortest and two longest sequences, and 32 more drawn at random
+    seqs = sorted(set([int(i) for i in order[:2]] + [int(i) for i in order[-2:]] +
+                      rng.choice(wl.num_seqs, 32, replace=False).tolist()))
+    assert len(seqs) >= 32
     ref = sampled_oracle(wl, vals, seqs)
     out, err = gpu_step(wl, vals)
     assert err == 0
@@ -63,13 +67,11 @@ def test_fragmented_mha_full_size_sampled(bs):
 def test_long_context_full_size_sampled():
     wl = W.config5()
     vals = W.make_values(wl, device=DEV, poison_tails=True)
-    seqs = [0, 11]
+    seqs = list(range(wl.num_seqs))  # all 16 sequences, every head
     ref = sampled_oracle(wl, vals, seqs)
     out, err = gpu_step(wl, vals)
     assert err == 0
     compare(out[seqs], ref, wl.name)
-    # every other row is at least finite and a convex mix of values
-    assert torch.isfinite(out.float()).all()
 
 
 LEN_MIX = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256,

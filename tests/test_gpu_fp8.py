@@ -2,8 +2,9 @@
 
 Cache writes and block copies must match the oracle byte for byte (the
 quantisation included); decode attention over the codes must meet the same
-bar as the bf16 path: every bf16 output within 1e-2 of the fp64 oracle over
-the same codes, every (sequence, head) row within 2e-2 relative L2 error."""
+bar as the bf16 path, element by element against the fp64 oracle over the
+same codes: |gpu - ref| <= 1e-2 and |gpu - ref| / max(|ref|, 1e-2) <= 2e-2,
+and every (sequence, head) row within 2e-2 relative L2 error."""
 import numpy as np
 import pytest
 import torch
@@ -113,7 +114,7 @@ def test_fp8_scales_apply():
 def test_fp8_long_context_full_size_sampled():
     wl = W.config5()
     vals = W.make_values_fp8(wl, device=DEV, poison_tails=True)
-    seqs = [0, 7, 15]
+    seqs = list(range(wl.num_seqs))  # all 16 sequences, every head
     ref = sampled_oracle(wl, vals, seqs, fp8_scales=(KS, VS))
     out, err = gpu_step_fp8(wl, vals, KS, VS)
     assert err == 0
