@@ -55,9 +55,6 @@
 
 namespace pa {
 
-#ifndef PA_WARP_BUDGET
-#define PA_WARP_BUDGET 16384
-#endif
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnit = 16;                           // tokens per pipeline stage
@@ -68,17 +65,11 @@ constexpr int kMaxParts = 1024;
 constexpr int kMaxSeqs = 8192;
 constexpr int kMaxGrid = 512;                       // persistent CTAs at most
 constexpr int kMaxWorkers = kMaxGrid * 4;           // balanced split: one worker per warp
-#ifndef PA_MIN_UNITS_PER_WORKER
-#define PA_MIN_UNITS_PER_WORKER 8
-#endif
-constexpr int kMinUnitsPerWorker = PA_MIN_UNITS_PER_WORKER;  // balanced split: work per warp at least
-#ifndef PA_PAIR_COST
-#define PA_PAIR_COST 4
-#endif
+constexpr int kMinUnitsPerWorker = 8;  // balanced split: work per warp at least
 // Balanced split: each (sequence, kv head) pair also costs this many units in
 // the stream being cut (its merge and bookkeeping), so a warp whose share holds
 // many short pairs gets fewer units.
-constexpr int kPairCost = PA_PAIR_COST;
+constexpr int kPairCost = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -112,7 +103,7 @@ struct Cfg {
   static constexpr int BOX_BYTES = KH * ROWS * 128;     // one box of K (or V), all halves
   static constexpr int KV_BYTES = BOXES * BOX_BYTES;    // K (or V) of a unit = 16 * D * 2
   static constexpr int STAGE = 2 * KV_BYTES;
-  static constexpr int BUDGET = NT == 1 ? PA_WARP_BUDGET : 16384;  // pipeline bytes per warp
+  static constexpr int BUDGET = 16384;  // pipeline bytes per warp
   static constexpr int STAGES_RAW = BUDGET / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr int HEADS = NT * 8;
@@ -588,41 +579,6 @@ __device__ __forceinline__ void attend_unit_fp8(uint32_t kb, uint32_t vb, int la
   }
 }
 
-#ifdef PA_TRACE
-// Per-CTA event log for timing studies: [cta][slot] = (event << 56) | ns.
-constexpr int kTraceSlots = 256;
-__device__ uint64_t g_trace[1024 * kTraceSlots];
-__device__ int g_trace_n[1024];
-#define PA_EVENT(ev)                                                              \
-  do {                                                                            \
-    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                  \
-      const int i_ = g_trace_n[blockIdx.x]++;                                     \
-      if (i_ < kTraceSlots)                                                       \
-        g_trace[blockIdx.x * kTraceSlots + i_] =                                  \
-            ((uint64_t)(ev) << 56) | (globaltimer_ns() & ((1ull << 56) - 1));     \
-    }                                                                             \
-  } while (0)
-// Per-warp log for the balanced-split kernel: [worker][slot].
-__device__ uint64_t g_wtrace[2048 * 16];
-__device__ int g_wtrace_n[2048];
-#define PA_WEVENT(w, ev)                                                          \
-  do {                                                                            \
-    if ((threadIdx.x & 31) == 0 && (w) < 2048) {                                  \
-      const int i_ = g_wtrace_n[w]++;                                             \
-      if (i_ < 16)                                                                \
-        g_wtrace[(w) * 16 + i_] =                                                 \
-            ((uint64_t)(ev) << 56) | (globaltimer_ns() & ((1ull << 56) - 1));     \
-    }                                                                             \
-  } while (0)
-#else
-#define PA_EVENT(ev) \
-  do {               \
-  } while (0)
-#define PA_WEVENT(w, ev) \
-  do {                   \
-  } while (0)
-#endif
-
 template <int D, int BS, int NT>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -664,7 +620,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   __syncthreads();
   const int total = prefix[a.num_seqs];
   const int G = a.group;
-  PA_EVENT(1);
 
   // This CTA's items are blockIdx.x, blockIdx.x + gridDim.x, then one per
   // dynamic fetch (2 * gridDim.x + counter).
@@ -760,7 +715,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
 #pragma unroll 1
   for (int k = 0; have_cur; ++k) {
-    PA_EVENT(2);
     // ---- fetch item k + 2 of this CTA; the value is only needed after the
     // merge, so it is published then and its latency hides behind the units
     int fetched = INT_MAX;
@@ -817,7 +771,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
       ++consumed;
     }
     fill();  // the next item's first units fly while the CTA merges
-    PA_EVENT(3);
     if (tid == 0) {
       mail[k & 3] = fetched;
       mbar_arrive(mail_bar + 8 * (k & 3));
@@ -910,7 +863,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     }
     __syncthreads();
 
-    PA_EVENT(4);
     const int64_t row0 = (int64_t)cur.s * a.n_q + (int64_t)cur.g * G;
     for (int i = tid; i < G * D; i += kThreads) {
       const int n = i / D, d = i - n * D;
@@ -927,7 +879,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
     __syncthreads();  // merge buffer, fin and misc are free again
     }  // cur.last
-    PA_EVENT(6);
 
     // ---- advance: the next item becomes current; learn the one after it
     have_cur = have_nxt;
@@ -963,7 +914,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   }
 
   __syncthreads();
-  PA_EVENT(7);
   griddep_launch_dependents();  // the partition merge may start launching
   if (tid == 0) {
     const int fin_ctas = atomicAdd(&a.work[1], 1);
@@ -974,12 +924,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
   }
 }
 
-#ifndef PA_SPLIT_BUDGET_FP8
-#define PA_SPLIT_BUDGET_FP8 8192  // stage-ring bytes per warp, E4M3 cache: 2 stages
-#endif
-#ifndef PA_SPLIT_BUDGET
-#define PA_SPLIT_BUDGET 16384
-#endif
+// Stage-ring bytes per warp of the balanced split: two stages of 16 tokens
+// of K and V (bf16: 2 x 8 KB at head_dim 128; E4M3: 2 x 4 KB).
+constexpr int kSplitRingBytes = 16384;
+constexpr int kSplitRingBytesFp8 = 8192;
 
 // Shared-memory layout of the balanced-split kernel: per-warp stage rings,
 // their mbarriers, a fault flag, then the prefix and length tables.
@@ -987,7 +935,7 @@ template <int D, int BS, int NT, bool FP8 = false>
 struct SplitCfg {
   using C = Cfg<D, BS, NT, FP8 ? 1 : 2>;
   static constexpr int STAGE = C::STAGE;
-  static constexpr int STAGES_RAW = (FP8 ? PA_SPLIT_BUDGET_FP8 : PA_SPLIT_BUDGET) / STAGE;
+  static constexpr int STAGES_RAW = (FP8 ? kSplitRingBytesFp8 : kSplitRingBytes) / STAGE;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
   static constexpr int MISC_OFF = BAR_OFF + kWarps * STAGES * 8;
@@ -1071,7 +1019,6 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       load_qf(qf_nxt, nxt);
     }
   }
-  PA_WEVENT(worker, 1);
   griddep_wait();  // from here on: pool reads, output and workspace writes
   // sequences with no tokens own no units: their outputs are zero
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x)
@@ -1161,7 +1108,6 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       fill();
       const uint32_t st = consumed % STAGES;
       wait_or_flag(my_bar + 8 * st, (consumed / STAGES) & 1u, a, fault);
-      if (consumed == 0) PA_WEVENT(worker, 2);  // first data
       const int nv = min(kUnit, cur.tok_end - (cur.u_begin + j) * kUnit);
       int cbid[BOXES];
 #pragma unroll
@@ -1200,7 +1146,6 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     fill();  // keep the ring full across the write below
 
     if (cur.last) {
-      PA_WEVENT(worker, 3);  // a segment's units done
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         lrun[t][0] = warp_sum_xor4(lrun[t][0]);
@@ -1267,15 +1212,6 @@ split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   }
 
-  PA_WEVENT(worker, 4);
-#ifdef PA_TRACE
-  {
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    if (lane == 0 && worker < 2048 && g_wtrace_n[worker] < 16)
-      g_wtrace[worker * 16 + g_wtrace_n[worker]++] = (5ull << 56) | smid;
-  }
-#endif
   __syncthreads();
   griddep_launch_dependents();  // the merge may start launching
 }
@@ -1298,12 +1234,8 @@ struct MergeArgs {
 };
 
 constexpr int kMergeWarps = 8;
-#ifndef PA_MERGE_PRE
-#define PA_MERGE_PRE 8  // parts a merge warp reads with the statistics, then per round
-#endif
-#ifndef PA_COOP_ROWS_PER_SM
-#define PA_COOP_ROWS_PER_SM 2  // a CTA per merge row up to this many rows per SM
-#endif
+constexpr int kMergePre = 8;       // parts a merge warp reads with the statistics, then per round
+constexpr int kCoopRowsPerSm = 2;  // a CTA per merge row up to this many rows per SM
 
 // The parts of merge row `row`: part q lives in partial row
 // q == 0 ? rfirst : rbase + q * rstep. Returns their number (0 or 1: the
@@ -1411,7 +1343,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
     auto rowq = [&](int q) -> long long { return q == 0 ? rfirst : rbase + q * rstep; };
     // One round trip for the statistics (lane q holds part q) and the first
     // kPre parts' rows; the rest stream kPre at a time.
-    constexpr int kPre = PA_MERGE_PRE;
+    constexpr int kPre = kMergePre;
     float2 st = make_float2(-INFINITY, 0.f);
     if (lane < nparts) st = __ldcg(&m.ws_ml[rowq(lane)]);
     float pre[kPre][PER];
@@ -1618,9 +1550,6 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
   st = a.balanced ? prepare(skern, smem, &cfg_split, occ_split, &occ)
                   : prepare(kern, smem, &cfg_item, occ_item, &occ);
   if (st != PA_OK) return st;
-#ifdef PA_MAX_CTAS_PER_SM
-  if (occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
-#endif
   int64_t grid = (int64_t)num_sms() * occ;
   if (!a.balanced && grid > items_upper) grid = items_upper;
   if (grid > kMaxGrid) grid = kMaxGrid;
@@ -1656,7 +1585,7 @@ static pa_status launch(DecodeArgs a, const void* k_pool, const void* v_pool,
     const int64_t rows = (int64_t)a.num_seqs * a.n_q;
     // Few rows (up to two per SM): a CTA per row, so that a row cut into many
     // parts is merged by eight warps; otherwise a warp per row.
-    m.coop = rows <= (long long)PA_COOP_ROWS_PER_SM * num_sms();
+    m.coop = rows <= (long long)kCoopRowsPerSm * num_sms();
     int64_t mgrid = m.coop ? rows : (rows + kMergeWarps - 1) / kMergeWarps;
     const int64_t mcap = (int64_t)num_sms() * 8;
     if (!m.coop && mgrid > mcap) mgrid = mcap;
@@ -1936,26 +1865,6 @@ static void* noalloc_scratch(pa_status* st) {
 }
 
 }  // namespace pa
-
-#ifdef PA_TRACE
-extern "C" int pa_trace_read(uint64_t* host, int* counts) {
-  if (cudaMemcpyFromSymbol(host, pa::g_trace, sizeof(pa::g_trace)) != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(counts, pa::g_trace_n, sizeof(pa::g_trace_n)) != cudaSuccess)
-    return -1;
-  static int zeros[2048] = {0};
-  if (cudaMemcpyToSymbol(pa::g_trace_n, zeros, sizeof(pa::g_trace_n)) != cudaSuccess) return -1;
-  return pa::kTraceSlots;
-}
-
-extern "C" int pa_wtrace_read(uint64_t* host, int* counts) {
-  if (cudaMemcpyFromSymbol(host, pa::g_wtrace, sizeof(pa::g_wtrace)) != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(counts, pa::g_wtrace_n, sizeof(pa::g_wtrace_n)) != cudaSuccess)
-    return -1;
-  static int zeros[2048] = {0};
-  if (cudaMemcpyToSymbol(pa::g_wtrace_n, zeros, sizeof(zeros)) != cudaSuccess) return -1;
-  return 16;
-}
-#endif
 
 extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool,
                                        const void* v_pool, const int32_t* block_tables,
