@@ -2,17 +2,22 @@
 
 A step is the whole hot path over one batch: copy-on-write block copies,
 the new tokens' K/V writes, and the paged decode attention (split-KV with a
-log-sum-exp merge). The default workload is the GQA decode batch (64
-sequences, lognormal lengths with median 300 clipped to [1, 2048], block 16,
-32 query / 8 kv heads, head_dim 128, bf16). Its pools fit in L2, so the
-timed steps rotate through enough independent replicas of the inputs that
-each step reads cold data.
+log-sum-exp merge).
 
 Metric: KV bytes the step must read (sum of lengths x kv heads x head_dim x
 2 bytes x K,V) per second of device time, plus tokens attended per second.
 
+With no workload flag, one line is printed per measured case (the block
+copy and the cache write on their own, every decode workload, the fp8
+cache, beam search, chunked prefill, swap) and the LAST line is the headline:
+the largest single-GPU decode workload, the fragmented MHA batch (256
+sequences of up to 4096 tokens, 32 query = 32 kv heads, head_dim 128, bf16,
+block 16, 8.6 GB of KV), with the roofline, the CPU baseline (the oracle)
+and the end-to-end figure.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 1..5] [--block-size 8|16|32] [--kv bf16|fp8]
+                    [--config 1..6] [--block-size 8|16|32] [--kv bf16|fp8]
+                    [--op decode|write|copy|prefill|swap]
 
 With --kv fp8 the pools hold E4M3 codes (one byte per element, per-tensor
 scales): the same step through the fp8 entry points, KV bytes halved.
@@ -42,6 +47,9 @@ PREFILL_SOURCES = ["paged_kv_cache_105_gb300/csrc/pa_prefill.cu",
                    "paged_kv_cache_105_gb300/csrc/pa_tc.cuh",
                    "paged_kv_cache_105_gb300/csrc/pa_ptx.cuh"]
 FALLBACK_HBM_GBS = 6800.0
+# The headline: the largest single-GPU decode workload (the fragmented MHA
+# batch, 8.6 GB of KV at block size 16).
+HEADLINE = (3, 16)
 
 
 def parse():
@@ -50,16 +58,20 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    p.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5, 6],
+                   help="one decode workload (default: every case, the headline last)")
     p.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32])
     p.add_argument("--partition-tokens", type=int, default=None)
     p.add_argument("--num-seqs", type=int, default=None,
                    help="configs 2-5: a smaller batch of the same shape (profiling)")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
-                   help="decode: the decode step (default); swap: block swap-out to pinned "
-                        "host memory and swap-in back; prefill: a chunked-prefill step")
+    p.add_argument("--op", choices=["decode", "write", "copy", "swap", "prefill"],
+                   default="decode",
+                   help="decode: the decode step (default); write: the cache write alone "
+                        "(the GQA batch's new tokens); copy: the copy-on-write block copy "
+                        "alone (the prefix-sharing batch's pairs); swap: block swap-out to "
+                        "pinned host memory and swap-in back; prefill: a chunked-prefill step")
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales)")
     p.add_argument("--eager", action="store_true",
@@ -273,7 +285,9 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = build_workload(args.config, args.block_size, args.num_seqs)
+    cfg = HEADLINE[0] if args.config is None else args.config
+    bs = HEADLINE[1] if args.config is None else args.block_size
+    wl = build_workload(cfg, bs, args.num_seqs)
     if hasattr(wl, "steps"):  # multi-step workload: the oracle times its first step
         wl = wl.steps[0]
     budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
@@ -347,21 +361,159 @@ def W_make_values_subset(wl, seqs, fp8=False):
     return {"wl": sub, "vals": vals, "seqs": list(range(len(seqs)))}
 
 
-def run_swap(args):
+class Env:
+    """The process's GPU, rank and library, set up once for every line."""
+
+    def __init__(self, args):
+        import torch
+        self.world, self.rank, self.local = dist_init(args)
+        self.dev = torch.device("cuda", self.local)
+        torch.cuda.set_device(self.dev)
+        import __graft_entry__
+        __graft_entry__.build()
+        self.l2 = torch.cuda.get_device_properties(self.dev).L2_cache_size
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+
+def release():
+    """Free the device memory of the line just measured before the next."""
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+class L2Flush:
+    """Between timed launches of a small kernel: a write over twice the L2
+    size, then a read of it (torch kernels), so that the kernel starts from
+    cold data and the L2 holds no dirty lines whose write-back would compete
+    with it."""
+
+    def __init__(self, env):
+        import torch
+        self.buf = torch.empty(2 * env.l2 // 4, dtype=torch.int32, device=env.dev)
+        self.sink = torch.empty((), dtype=torch.int32, device=env.dev)
+
+    def __call__(self):
+        import torch
+        self.buf.fill_(1)
+        torch.amax(self.buf, dim=0, out=self.sink)
+
+
+def time_small_kernel(env, fn, reps):
+    """Median CUDA-event time (ms) of one launch of `fn` after an L2 flush,
+    over `reps` launches, on the current stream."""
+    import torch
+    flush = L2Flush(env)
+    stream = torch.cuda.current_stream(env.dev)
+    for _ in range(5):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def small_op_line(args, env, what, wl, bytes_moved, ms, launches, note, kernel):
+    peak, peak_kind = measured_peak()
+    ms = max_over_ranks(ms, env.world, env.dev)
+    gbs = whole_job_rate(bytes_moved, env.world, ms * 1e-3) / 1e9
+    return {"metric": f"{what} read+write GB/s", "value": gbs, "unit": "GB/s",
+            "n_gpus": env.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8 (bit copy)", "data": "synthetic",
+            "config": {"workload": wl.name, "bytes_per_launch": bytes_moved,
+                       "l2": "L2 flushed (a 2x L2 write, then a read of it) before every "
+                             "timed launch",
+                       "timing": f"median of {args.steps} launches, CUDA events around each"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "kernel": kernel,
+                         "peak_source": f"{peak_kind} hbm_gbs", "note": note},
+            "gpu_launches": launches}
+
+
+def run_write(args, env):
+    """a2 alone: the GQA batch's new tokens written into their slots."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_105_gb300 import binding as B
+    from paged_kv_cache_105_gb300 import workloads as W
+    wl = W.config2()
+    vals = W.make_values(wl, device=env.dev)
+    sm = torch.from_numpy(np.ascontiguousarray(wl.slot_mapping)).to(env.dev)
+    err = torch.zeros(1, dtype=torch.int32, device=env.dev)
+
+    def fn():
+        B.pa_reshape_and_cache(vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"], sm,
+                               err_word=err)
+
+    ms = time_small_kernel(env, fn, args.steps)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+    row = wl.n_kv_heads * wl.head_dim * 2
+    nbytes = 2 * 2 * wl.num_seqs * row + 4 * wl.num_seqs  # K, V read and written; slots
+    us = ms * 1e3
+    note = (f"launch-bound: {nbytes / 1e3:.0f} kB per launch would take "
+            f"{nbytes / (measured_peak()[0] * 1e3):.2f} us at the copy peak; the launch "
+            f"and its latency take the rest of {us:.1f} us")
+    line = small_op_line(args, env, "reshape_and_cache (new tokens' K/V into the pool)", wl,
+                         nbytes, ms, args.steps, note, "reshape_and_cache_kernel (pa_reshape_and_cache)")
+    line["config"]["tokens"] = wl.num_seqs
+    return line
+
+
+def run_copy(args, env):
+    """a1 alone: the prefix-sharing batch's copy-on-write block copies."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_105_gb300 import binding as B
+    from paged_kv_cache_105_gb300 import workloads as W
+    wl = W.config4()
+    vals = W.make_values(wl, device=env.dev)
+    pairs = torch.from_numpy(np.ascontiguousarray(wl.cow_pairs.reshape(-1, 2))).to(env.dev)
+    err = torch.zeros(1, dtype=torch.int32, device=env.dev)
+
+    def fn():
+        B.pa_copy_blocks(vals["k_pool"], vals["v_pool"], pairs, err_word=err)
+
+    ms = time_small_kernel(env, fn, args.steps)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+    n = int(wl.cow_pairs.shape[0])
+    block = wl.n_kv_heads * wl.block_size * wl.head_dim * 2
+    nbytes = 2 * 2 * n * block + 8 * n  # K and V blocks read and written; pairs
+    note = (f"{n} pairs, {nbytes / 1e6:.1f} MB per launch: {nbytes / (measured_peak()[0] * 1e3):.2f}"
+            f" us at the copy peak; launch latency is a large share of {ms * 1e3:.1f} us")
+    line = small_op_line(args, env, "copy_blocks (copy-on-write block copies)", wl, nbytes, ms,
+                         args.steps, note, "copy_blocks_kernel (pa_copy_blocks)")
+    line["config"]["pairs"] = n
+    return line
+
+
+def run_swap(args, env):
     """Preemption by swapping: every block the workload's tables use goes to a
     pinned host pool (swap-out) and comes back to the same ids (swap-in);
     one step = both. Compared with the copy engine moving the same bytes as
     one contiguous buffer each way (torch copy_, device <-> pinned host)."""
     import numpy as np
     import torch
-    world, rank, local = dist_init(args)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    import __graft_entry__
-    __graft_entry__.build()
     from paged_kv_cache_105_gb300 import binding as B
     from paged_kv_cache_105_gb300 import workloads as W
-    wl = build_workload(args.config, args.block_size, args.num_seqs)
+    dev = env.dev
+    cfg = 2 if args.config is None else args.config
+    wl = build_workload(cfg, args.block_size, args.num_seqs)
     fp8 = fp8_scale_of(args)
     vals = W.make_values_fp8(wl, device=dev) if fp8 is not None else W.make_values(wl, device=dev)
     gk, gv = vals["k_pool"], vals["v_pool"]
@@ -387,7 +539,7 @@ def run_swap(args):
         hbuf.copy_(dbuf, non_blocking=True)
         dbuf.copy_(hbuf, non_blocking=True)
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(env.local)
     clocks.start()
     res = {}
     for name, fn in (("kernel", step), ("copy_engine", ce_step)):
@@ -404,42 +556,35 @@ def run_swap(args):
     clk = clocks.stop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
-    res = {k: max_over_ranks(v, world, dev) for k, v in res.items()}
-    if rank != 0:
-        return
+    res = {k: max_over_ranks(v, env.world, dev) for k, v in res.items()}
+    world = env.world
     gbs = whole_job_rate(moved, world, res["kernel"] * 1e-3) / 1e9
     ce = whole_job_rate(moved, world, res["copy_engine"] * 1e-3) / 1e9
-    line = {"metric": "KV block swap, device <-> pinned host (out + in) GB/s", "value": gbs,
+    return {"metric": "KV block swap, device <-> pinned host (out + in) GB/s", "value": gbs,
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": res["kernel"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8 (byte copy)", "data": "synthetic",
             "config": {"workload": wl.name, "kv_dtype": args.kv, "blocks": n,
                        "block_bytes": block_bytes, "bytes_per_step": moved,
-                       "l2": f"{moved / 2e6:.0f} MB per direction vs "
-                             f"{torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB L2"},
+                       "l2": f"{moved / 2e6:.0f} MB per direction vs {env.l2 / 1e6:.0f} MB L2"},
             "roofline": {"bound": "chip-to-chip link", "achieved": gbs, "peak": ce,
                          "unit": "GB/s", "frac": gbs / ce, "traffic": None,
                          "kernel": "swap_blocks_kernel (pa_swap_blocks) x2",
                          "peak_source": "copy engine moving the same bytes as one contiguous "
                                         "buffer each way, measured in this run"},
             "gpu_launches": 2 * args.steps, "clocks": clk}
-    print(json.dumps(line), flush=True)
 
 
-def run_prefill(args):
+def run_prefill(args, env):
     """One chunked-prefill step = the chunk tokens' cache write + causal
     attention of every chunk token over its whole paged context. Metric:
     causal attention flops per second (4 * head_dim * query heads per visible
     (token, position) pair) against the measured bf16 tensor peak."""
     import numpy as np
     import torch
-    world, rank, local = dist_init(args)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    import __graft_entry__
-    __graft_entry__.build()
     from paged_kv_cache_105_gb300 import binding as B
     from paged_kv_cache_105_gb300 import workloads as W
+    dev = env.dev
     wl = W.prefill_chunked()
     vals = W.make_prefill_values(wl, device=dev)
     t = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).to(dev)
@@ -467,7 +612,7 @@ def run_prefill(args):
     with torch.cuda.graph(ga, stream=cap):
         attend()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(env.local)
     clocks.start()
     for _ in range(max(3, args.warmup)):
         gs.replay()
@@ -476,26 +621,31 @@ def run_prefill(args):
     while time.perf_counter() - t_pre < 1.0:
         gs.replay()
         torch.cuda.synchronize()
+    env.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         gs.replay()
     e1.record(stream)
     torch.cuda.synchronize()
+    env.barrier()
+    # the prefill kernel alone: one event pair around 4 back-to-back replays,
+    # repeated; the median per launch
+    inner, reps = 4, max(20, min(50, args.steps))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(reps)]
     for a_, b_ in evs:
         a_.record(stream)
-        ga.replay()
+        for _ in range(inner):
+            ga.replay()
         b_.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
+    world = env.world
     step_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-    att_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
-    if rank != 0:
-        return
+    att_ms = statistics.median(a_.elapsed_time(b_) / inner for a_, b_ in evs)
     flops = wl.flops()
     value = whole_job_rate(flops, world, step_ms * 1e-3) / 1e12
     achieved = flops / (att_ms * 1e-3) / 1e12
@@ -507,7 +657,7 @@ def run_prefill(args):
             kind = "measured"
     if not peak:
         peak = 1900.0
-    line = {"metric": "chunked-prefill causal attention TFLOP/s", "value": value,
+    return {"metric": "chunked-prefill causal attention TFLOP/s", "value": value,
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -525,46 +675,34 @@ def run_prefill(args):
                                                      PREFILL_SOURCES),
                          "kernel": "prefill_tc_kernel (pa_prefill)",
                          "peak_source": f"{kind} bf16_tflops (cuBLAS, burst)",
-                         "prefill_ms_avg": att_ms},
+                         "timing": f"one CUDA event pair around {inner} back-to-back "
+                                   f"prefill-only graph replays, median of {reps}",
+                         "prefill_ms": att_ms},
             "gpu_launches": 2 * args.steps, "clocks": clk}
-    print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        run_reference(args)
-        return
-    if args.op == "swap":
-        run_swap(args)
-        return
-    if args.op == "prefill":
-        run_prefill(args)
-        return
-
+def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=None,
+               cpu_baseline=False, e2e_steps=None):
+    """The decode step of workload `cfg` (copy-on-write copies, the new
+    tokens' writes, the decode and its merge) timed K times; returns the
+    JSON line (rank 0) or None."""
     import numpy as np
     import torch
-
-    world, rank, local = dist_init(args)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    import __graft_entry__
-    __graft_entry__.build()
     from paged_kv_cache_105_gb300 import binding as B
     from paged_kv_cache_105_gb300 import workloads as W
+    world, rank, dev = env.world, env.rank, env.dev
 
     # A workload is a list of decode steps over one pool: one step for the
     # single-step batches, T steps (forks, frees, copy-on-write between them)
     # for beam search; the timed steps cycle through them.
-    wl0 = build_workload(args.config, args.block_size, args.num_seqs)
+    wl0 = build_workload(cfg, bs, num_seqs)
     multi = isinstance(wl0, W.MultiStep)
     steps_wl = wl0.steps if multi else [wl0]
     wl = steps_wl[0]
     name = wl0.name
     T = len(steps_wl)
-    fp8 = fp8_scale_of(args)
-    P = wl.partition_tokens if args.partition_tokens is None else args.partition_tokens
+    fp8 = W.FP8_SCALE if kv == "fp8" else None
+    P = wl.partition_tokens if partition_tokens is None else partition_tokens
     if fp8 is not None:
         P = 0  # the fp8 decode always runs the balanced split
     msl = max(w.max_seq_len for w in steps_wl)
@@ -575,7 +713,7 @@ def main():
                  [W.make_step_values(w, device=dev) for w in steps_wl])
     pools0 = {k: base[k] for k in ("k_pool", "v_pool")}
     pool_bytes = 2 * base["k_pool"].numel() * eb
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    l2 = env.l2
     kv_min = min(w.kv_bytes(eb) for w in steps_wl)
     replicas = 1 if multi else max(1, math.ceil(3 * l2 / max(1, kv_min)))
     replicas = min(replicas, max(1, int(40e9 // max(1, pool_bytes))))
@@ -665,18 +803,8 @@ def main():
         if ev is not None:
             ev[1].record(stream)
 
-    def decode_only(i, ev):
-        ev[0].record(stream)
-        graphs[which(i)][1].replay()
-        ev[1].record(stream)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     # Warm up with continuous load long enough for the clock sampler to see it.
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(env.local)
     clocks.start()
     for i in range(max(3, args.warmup)):
         step(i)
@@ -688,10 +816,10 @@ def main():
             step(i)
             i += 1
         torch.cuda.synchronize()
-    barrier()
+    env.barrier()
     torch.cuda.synchronize()
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    dec_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if graphs is None else [None] * args.steps)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -699,12 +827,34 @@ def main():
         step(k, dec_ev[k])
     t1.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    env.barrier()
+    # The decode on its own, for the roofline: one event pair around `inner`
+    # back-to-back decode-only graph replays (cycling the replicas, so every
+    # launch reads cold data), repeated; per repeat the algorithmic bytes of
+    # its launches over its time, and the median over the repeats.
+    inner = max(replicas, 8)
+    roof_reps = 50
+    roof = []
     if graphs is not None:
-        # the decode kernel on its own, K launches, for the roofline
-        for k in range(args.steps):
-            decode_only(k, dec_ev[k])
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(roof_reps)]
+        idx = 0
+        groups = []
+        for a_, b_ in evs:
+            a_.record(stream)
+            g = []
+            for _ in range(inner):
+                graphs[which(idx)][1].replay()
+                g.append(idx)
+                idx += 1
+            b_.record(stream)
+            groups.append(g)
         torch.cuda.synchronize()
+        for (a_, b_), g in zip(evs, groups):
+            ms = a_.elapsed_time(b_)
+            nb = sum(steps_wl[which(x)[1]].kv_bytes(eb) + steps_wl[which(x)[1]].io_bytes()
+                     for x in g)
+            roof.append((ms / inner, nb / (ms * 1e-3) / 1e9))
     # keep the load on a little past the timed region for the sampler
     t_post = time.perf_counter()
     while time.perf_counter() - t_post < 0.3:
@@ -717,7 +867,6 @@ def main():
         raise RuntimeError(f"device error word {int(err.item()):#x}")
 
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
 
     timed = [steps_wl[i % T] for i in range(args.steps)]
     kv_total = sum(w.kv_bytes(eb) for w in timed)
@@ -730,21 +879,21 @@ def main():
     tokens_per_s = whole_job_rate(tok_total, world, total_ms * 1e-3)
 
     # ---- end to end through the public API, host buffers, copies timed
-    e2e_steps = args.e2e_steps or max(10, min(200, args.steps))
+    e2e_steps = e2e_steps or args.e2e_steps or max(10, min(200, args.steps))
     # Each step's inputs (the new tokens' q, k, v and the index arrays) sit in
     # one page-locked host buffer, 256-byte aligned pieces, and go to the GPU
     # in one copy into a device staging buffer the calls read through views,
     # as a serving engine stages a step's inputs.
     def pack(tensors):
         lay, off = {}, 0
-        for name, t in tensors.items():
+        for key, t in tensors.items():
             nb = t.numel() * t.element_size()
-            lay[name] = (off, t.dtype, tuple(t.shape), nb)
+            lay[key] = (off, t.dtype, tuple(t.shape), nb)
             off += (nb + 255) // 256 * 256
         buf = torch.empty(max(off, 256), dtype=torch.uint8, pin_memory=True)
-        for name, (o, _, _, nb) in lay.items():
+        for key, (o, _, _, nb) in lay.items():
             if nb:
-                buf[o:o + nb].copy_(tensors[name].contiguous().reshape(-1).view(torch.uint8))
+                buf[o:o + nb].copy_(tensors[key].contiguous().reshape(-1).view(torch.uint8))
         return buf, lay
 
     host_pack, layouts = [], []
@@ -756,8 +905,8 @@ def main():
         host_pack.append(buf)
         layouts.append(lay)
     stage = torch.empty(max(b.numel() for b in host_pack), dtype=torch.uint8, device=dev)
-    dev_views = [{name: stage[o:o + nb].view(dt).view(shape)
-                  for name, (o, dt, shape, nb) in lay.items()} for lay in layouts]
+    dev_views = [{key: stage[o:o + nb].view(dt).view(shape)
+                  for key, (o, dt, shape, nb) in lay.items()} for lay in layouts]
     host_out = torch.empty(base["q"].shape, dtype=torch.bfloat16, pin_memory=True)
     h2d_steps, d2h = [], host_out.numel() * host_out.element_size()
     cur_stream = torch.cuda.current_stream(dev)
@@ -775,23 +924,34 @@ def main():
 
     for i in range(3):
         e2e_step(i)
-    barrier()
+    env.barrier()
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for i in range(e2e_steps):
         h2d_steps.append(e2e_step(i))
     w1 = time.perf_counter()
-    barrier()
+    env.barrier()
     e2e_s = max_over_ranks(w1 - w0, world, dev)
     e2e_value = whole_job_rate(sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)),
                                world, e2e_s) / 1e9
     h2d = sum(h2d_steps) / len(h2d_steps)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
 
     if rank != 0:
-        return
+        return None
 
     peak, peak_kind = measured_peak()
-    achieved = alg_total / (sum(dec_ms) * 1e-3) / 1e9
+    if roof:
+        dec_ms = statistics.median(r[0] for r in roof)
+        achieved = statistics.median(r[1] for r in roof)
+        timing = (f"one CUDA event pair around {inner} back-to-back decode-only graph "
+                  f"replays (replicas cycled), median over {len(roof)} repeats")
+    else:
+        per = [a.elapsed_time(b) for a, b in dec_ev]
+        dec_ms = statistics.median(per)
+        achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
+        timing = "CUDA events around each decode launch inside the timed steps, median"
     traffic = recorded_traffic(name + ("-fp8" if fp8 is not None else ""))
     kname = ("split_kernel<fp8> (pa_decode_fp8) + merge_kernel" if fp8 is not None else
              "split_kernel (pa_decode, balanced split) + merge_kernel" if P == 0 else
@@ -801,14 +961,14 @@ def main():
                 "kernel": kname,
                 "peak_source": f"{peak_kind} hbm_gbs",
                 "alg_bytes_per_launch": alg_bytes,
-                "timing": ("CUDA events around each decode launch inside the timed steps"
-                           if args.eager else
-                           f"CUDA events around each of {args.steps} decode-graph replays "
-                           "right after the timed steps (same inputs, same replicas)"),
-                "decode_ms_avg": sum(dec_ms) / len(dec_ms)}
+                "timing": timing,
+                "decode_ms": dec_ms}
+    if multi or cfg == 4:
+        roofline["note"] = ("logical bytes: shared blocks are read once per sequence that maps "
+                            "them, mostly from L2 (L2-assisted); traffic gives the DRAM bytes")
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if cpu_baseline and world == 1:
         budget = 6000 if wl.n_q_heads * wl.head_dim >= 4096 else 20000
         seqs, tok = cpu_sample_seqs(wl, budget)
         sub = W_make_values_subset(wl, seqs, fp8=fp8 is not None)
@@ -846,7 +1006,7 @@ def main():
     if multi:
         unique = [u * 2 * wl.n_kv_heads * wl.block_size * wl.head_dim * eb
                   for u in wl0.used_blocks]
-    config = {"workload": name, "kv_dtype": args.kv, "num_seqs": wl.num_seqs,
+    config = {"workload": name, "kv_dtype": kv, "num_seqs": wl.num_seqs,
               "tokens_attended": int(tok_total / args.steps), "n_q_heads": wl.n_q_heads,
               "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
               "block_size": wl.block_size, "partition_tokens": P_res,
@@ -857,10 +1017,11 @@ def main():
                      f"one pool; {kv_bytes / 1e6:.0f} MB of KV read per step (logical) over "
                      f"{max(unique) / 1e6:.0f} MB of unique blocks vs {l2 / 1e6:.0f} MB L2: "
                      "L2-assisted"),
-              "arithmetic": ("bf16 operands, fp32 accumulation and softmax"
+              "arithmetic": ("bf16 operands, fp32 accumulation and softmax; P as a bf16 "
+                             "hi + lo pair (two P V products)"
                              if fp8 is None else
                              "E4M3 codes and q as f16 mma operands, fp32 accumulation "
-                             "and softmax; per-tensor scales"),
+                             "and softmax; P as an f16 hi + lo pair; per-tensor scales"),
               "launch": "eager calls from Python" if args.eager else
                         "one CUDA graph replay per step (copy, write, decode, merge)",
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
@@ -871,7 +1032,7 @@ def main():
         config["sharing"] = {"used_blocks_last": wl0.used_blocks[-1],
                              "unshared_blocks_last": wl0.unshared_blocks[-1],
                              "saving": 1 - wl0.used_blocks[-1] / wl0.unshared_blocks[-1]}
-    line = {
+    return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -890,7 +1051,64 @@ def main():
         "gpu_launches": sum(launches[i % T] for i in range(args.steps)),
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+
+
+def emit(line, env):
+    if line is not None and env.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def suite(args, env):
+    """Every measured case, one line each; the headline last."""
+    cases = [
+        lambda: run_copy(args, env),
+        lambda: run_write(args, env),
+        lambda: run_decode(args, env, 1, 16, e2e_steps=20),
+        lambda: run_decode(args, env, 2, 16, e2e_steps=50),
+        lambda: run_decode(args, env, 2, 16, kv="fp8", e2e_steps=50),
+        lambda: run_decode(args, env, 4, 16, e2e_steps=20),
+        lambda: run_decode(args, env, 5, 16, e2e_steps=10),  # 512-token partitions
+        lambda: run_decode(args, env, 5, 16, partition_tokens=0, e2e_steps=10),
+        lambda: run_decode(args, env, 5, 16, kv="fp8", e2e_steps=10),
+        lambda: run_decode(args, env, 6, 16, e2e_steps=20),
+        lambda: run_decode(args, env, 3, 8, e2e_steps=10),
+        lambda: run_decode(args, env, 3, 32, e2e_steps=10),
+        lambda: run_prefill(args, env),
+        lambda: run_swap(args, env),
+    ]
+    for case in cases:
+        emit(case(), env)
+        release()
+    emit(run_decode(args, env, HEADLINE[0], HEADLINE[1], cpu_baseline=not args.no_cpu_baseline),
+         env)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    env = Env(args)
+    if args.op == "swap":
+        emit(run_swap(args, env), env)
+    elif args.op == "prefill":
+        emit(run_prefill(args, env), env)
+    elif args.op == "write":
+        emit(run_write(args, env), env)
+    elif args.op == "copy":
+        emit(run_copy(args, env), env)
+    elif args.config is None:
+        if args.num_seqs is not None or args.partition_tokens is not None or args.kv != "bf16":
+            # a flag that shapes one decode workload: the headline workload with it
+            emit(run_decode(args, env, HEADLINE[0], args.block_size, kv=args.kv,
+                            partition_tokens=args.partition_tokens, num_seqs=args.num_seqs,
+                            cpu_baseline=not args.no_cpu_baseline), env)
+        else:
+            suite(args, env)
+    else:
+        emit(run_decode(args, env, args.config, args.block_size, kv=args.kv,
+                        partition_tokens=args.partition_tokens, num_seqs=args.num_seqs,
+                        cpu_baseline=not args.no_cpu_baseline), env)
 
 
 if __name__ == "__main__":
