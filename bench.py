@@ -908,33 +908,72 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
     dev_views = [{key: stage[o:o + nb].view(dt).view(shape)
                   for key, (o, dt, shape, nb) in lay.items()} for lay in layouts]
     host_out = torch.empty(base["q"].shape, dtype=torch.bfloat16, pin_memory=True)
-    h2d_steps, d2h = [], host_out.numel() * host_out.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     cur_stream = torch.cuda.current_stream(dev)
+    # The public prepared-step object: checks and argument lists built once.
+    dsteps = {}
+    for j in range(replicas):
+        for k in range(T):
+            v = dev_views[k]
+            dsteps[(j, k)] = B.DecodeStep(
+                outs[j], v["q"], reps[j]["k_pool"], reps[j]["v_pool"], v["bt"], v["sl"],
+                wl.scale, max_seq_len=msl, workspace=wss[j], k_new=v["k_new"], v_new=v["v_new"],
+                slot_mapping=v["sm"], pairs=v["pairs"] if npairs[k] else None,
+                partition_tokens=P, err_word=err,
+                kv_scales=(fp8, fp8) if fp8 is not None else None)
 
-    def e2e_step(i):
-        j, k = which(i)
+    def e2e_body(j, k):
         hb = host_pack[k]
         stage[:hb.numel()].copy_(hb, non_blocking=True)
-        v = dev_views[k]
-        api_write(reps[j], k, v["pairs"], v["k_new"], v["v_new"], v["sm"])
-        api_decode(outs[j], v["q"], reps[j], v["bt"], v["sl"], wss[j])
+        dsteps[(j, k)].enqueue()
         host_out.copy_(outs[j], non_blocking=True)
-        cur_stream.synchronize()  # the caller needs the result
-        return hb.numel()
 
-    for i in range(3):
-        e2e_step(i)
-    env.barrier()
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for i in range(e2e_steps):
-        h2d_steps.append(e2e_step(i))
-    w1 = time.perf_counter()
-    env.barrier()
-    e2e_s = max_over_ranks(w1 - w0, world, dev)
-    e2e_value = whole_job_rate(sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)),
-                               world, e2e_s) / 1e9
-    h2d = sum(h2d_steps) / len(h2d_steps)
+    def e2e_eager(i):
+        e2e_body(*which(i))
+        cur_stream.synchronize()  # the caller needs the result
+
+    # The same step captured once per (replica, step) as a CUDA graph: the
+    # input copy, the three library calls and the output copy, replayed and
+    # synchronised every step, as a serving engine replays its decode step.
+    e2e_graphs, graph_note = None, None
+    try:
+        e2e_graphs = {}
+        cap2 = torch.cuda.Stream(dev)
+        for j in range(replicas):
+            for k in range(T):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap2):
+                    e2e_body(j, k)
+                e2e_graphs[(j, k)] = g
+        torch.cuda.synchronize()
+    except Exception as ex:  # capture of the host copies refused: eager only
+        e2e_graphs, graph_note = None, f"graph capture failed ({type(ex).__name__}: {ex})"
+        torch.cuda.synchronize()
+
+    def e2e_graphed(i):
+        e2e_graphs[which(i)].replay()
+        cur_stream.synchronize()
+
+    def time_e2e(fn):
+        for i in range(3):
+            fn(i)
+        env.barrier()
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        for i in range(e2e_steps):
+            fn(i)
+        w1 = time.perf_counter()
+        env.barrier()
+        sec = max_over_ranks(w1 - w0, world, dev)
+        return whole_job_rate(sum(steps_wl[i % T].kv_bytes(eb) for i in range(e2e_steps)),
+                              world, sec) / 1e9, sec / e2e_steps
+
+    eager_value, eager_s = time_e2e(e2e_eager)
+    if e2e_graphs is not None:
+        e2e_value, e2e_step_s = time_e2e(e2e_graphed)
+    else:
+        e2e_value, e2e_step_s = eager_value, eager_s
+    h2d = sum(host_pack[which(i)[1]].numel() for i in range(e2e_steps)) / e2e_steps
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
 
@@ -1045,9 +1084,18 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e2e_step_s * 1e3,
+                "launch": ("one CUDA graph replay per step (input copy, DecodeStep.enqueue: "
+                           "copy_blocks, reshape_and_cache, decode, merge; output copy), "
+                           "then a stream synchronise" if e2e_graphs is not None else
+                           graph_note),
+                "eager": {"value": eager_value, "ms_per_step": eager_s * 1e3,
+                          "launch": "the same calls issued from Python every step "
+                                    "(DecodeStep.enqueue), then a stream synchronise"},
                 "note": "every step: its inputs (q, k, v of the new tokens, block tables, "
                         "lengths, slots, copy pairs) copied in from one page-locked buffer, "
-                        "the public calls, the output copied out, synchronised"},
+                        "the public calls, the output copied out to page-locked memory, "
+                        "synchronised"},
         "gpu_launches": sum(launches[i % T] for i in range(args.steps)),
         "clocks": clk,
     }

@@ -393,3 +393,101 @@ def pa_swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, err_word=None, stream=N
                               _ptr(err_word), _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_swap_blocks", st)
+
+
+# ------------------------------------------------------------ prepared step
+
+class DecodeStep:
+    """One decode step of a fixed batch shape, prepared once: the
+    copy-on-write block copies (if `pairs` has rows), the new tokens' cache
+    write, and the decode with its merge, in that order on one stream.
+
+    Every check and every pointer extraction happens here, once; enqueue()
+    makes only the three library calls, with argument lists built in the
+    constructor. The step reads whatever the given tensors hold when it runs,
+    so a serving loop refreshes q, the new K/V, the tables, lengths, slots and
+    pairs in place between steps (their shapes and storage must not change,
+    and they must outlive this object). kv_scales = (k_scale, v_scale) selects
+    the E4M3 entry points (uint8 pools). A CUDA graph may capture enqueue().
+    """
+
+    def __init__(self, out, q, k_pool, v_pool, block_tables, seq_lens, scale, *, max_seq_len,
+                 workspace, k_new, v_new, slot_mapping, pairs=None, partition_tokens=0,
+                 err_word=None, kv_scales=None, stream=None):
+        fp8 = kv_scales is not None
+        dev = q.device
+        pool_t = torch.uint8 if fp8 else torch.bfloat16
+        _check(q, "q", torch.bfloat16, 3)
+        _check(out, "out", torch.bfloat16, 3, dev)
+        _check(k_pool, "k_pool", pool_t, 4, dev)
+        _check(v_pool, "v_pool", pool_t, 4, dev)
+        _check(block_tables, "block_tables", torch.int32, 2, dev)
+        _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+        _check(workspace, "workspace", torch.uint8, 1, dev)
+        _check(k_new, "k_new", torch.bfloat16, 3, dev)
+        _check(v_new, "v_new", torch.bfloat16, 3, dev)
+        _check(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+        if pairs is not None:
+            _check(pairs, "pairs", torch.int32, 2, dev)
+            if pairs.numel() and pairs.shape[1] != 2:
+                raise ValueError("pairs must be [n, 2]")
+        if err_word is not None:
+            _check(err_word, "err_word", torch.int32, None, dev)
+        S, Hq, D = q.shape
+        NB, Hkv, bs, D2 = k_pool.shape
+        T = k_new.shape[0]
+        if tuple(out.shape) != (S, Hq, D) or D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+            raise ValueError("shape mismatch between q, out and the pools")
+        if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+            raise ValueError("block_tables / seq_lens must have one row per sequence")
+        if tuple(k_new.shape) != (T, Hkv, D) or v_new.shape != k_new.shape:
+            raise ValueError("new K/V must be [tokens, n_kv_heads, head_dim]")
+        if slot_mapping.shape[0] != T:
+            raise ValueError("slot_mapping must have one entry per new token")
+        L = lib()
+        self._tensors = (out, q, k_pool, v_pool, block_tables, seq_lens, workspace, k_new,
+                         v_new, slot_mapping, pairs, err_word)  # kept alive
+        self._dev = dev.index if dev.index is not None else torch.cuda.current_device()
+        self._fixed_stream = None if stream is None else _stream(stream, dev)
+        err = _ptr(err_word)
+        n_pairs = 0 if pairs is None else pairs.shape[0]
+        self._copy = None
+        if n_pairs:
+            fn = L.pa_copy_blocks_fp8 if fp8 else L.pa_copy_blocks
+            self._copy = (fn, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks",
+                          (_ptr(k_pool), _ptr(v_pool), _ptr(pairs), n_pairs, Hkv, D, bs, NB,
+                           err))
+        if fp8:
+            ks, vs = float(kv_scales[0]), float(kv_scales[1])
+            self._write = (L.pa_reshape_and_cache_fp8, "pa_reshape_and_cache_fp8",
+                           (_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                            _ptr(slot_mapping), T, NB, Hkv, D, bs, ks, vs, err))
+            self._decode = (L.pa_decode_fp8, "pa_decode_fp8",
+                            (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                             _ptr(seq_lens), S, block_tables.shape[1], NB, Hq, Hkv, D, bs,
+                             float(scale), ks, vs, int(max_seq_len), _ptr(workspace),
+                             workspace.numel(), err))
+        else:
+            self._write = (L.pa_reshape_and_cache, "pa_reshape_and_cache",
+                           (_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                            _ptr(slot_mapping), T, NB, Hkv, D, bs, err))
+            self._decode = (L.pa_decode, "pa_decode",
+                            (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                             _ptr(seq_lens), S, block_tables.shape[1], NB, Hq, Hkv, D, bs,
+                             float(scale), int(partition_tokens), int(max_seq_len),
+                             _ptr(workspace), workspace.numel(), err))
+
+    def enqueue(self):
+        """Issue the step on the stream given at construction, else on the
+        current stream of the tensors' device."""
+        st = self._fixed_stream
+        if st is None:
+            st = (_raw_stream(self._dev) if _raw_stream is not None else
+                  torch.cuda.current_stream(self._dev).cuda_stream)
+        for call in (self._copy, self._write, self._decode):
+            if call is None:
+                continue
+            fn, name, args = call
+            r = fn(*args, st)
+            if r != PA_OK:
+                raise PAError(name, r)

@@ -261,3 +261,42 @@ def test_rising_scores_move_the_running_max(partition_tokens):
     out, err = gpu_step(wl, on_dev(vals_cpu), partition_tokens=partition_tokens)
     assert err == 0
     compare(out, ref, "rising")
+
+
+def test_prepared_step_matches_the_oracle_eager_and_graphed():
+    # DecodeStep: copy-on-write copies, cache write and decode from argument
+    # lists built once; then the same object captured in a CUDA graph.
+    from tests.helpers import to_dev
+    wl = W.config4()
+    assert len(wl.cow_pairs) > 0
+    vals_cpu = W.make_values(wl, poison_tails=True)
+    ref, kp, vp = oracle_step(wl, vals_cpu)
+    vals = on_dev(vals_cpu)
+    t = to_dev(wl, DEV)
+    ws = B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                            wl.block_size, wl.max_seq_len, wl.partition_tokens, device=DEV)
+    out = torch.full_like(vals["q"], float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    step = B.DecodeStep(out, vals["q"], vals["k_pool"], vals["v_pool"], t["block_tables"],
+                        t["seq_lens"], wl.scale, max_seq_len=wl.max_seq_len, workspace=ws,
+                        k_new=vals["k_new"], v_new=vals["v_new"],
+                        slot_mapping=t["slot_mapping"], pairs=t["pairs"],
+                        partition_tokens=wl.partition_tokens, err_word=err)
+    step.enqueue()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(bits(vals["k_pool"]), kp)
+    assert np.array_equal(bits(vals["v_pool"]), vp)
+    compare(out, ref, wl.name + "-prepared")
+    first = out.clone()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(DEV)
+    with torch.cuda.graph(g, stream=cap):
+        step.enqueue()
+    out.fill_(float("nan"))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+    assert np.array_equal(bits(vals["k_pool"]), kp)

@@ -169,3 +169,26 @@ def test_fp8_rising_scores_move_the_running_max():
     out, err = gpu_step_fp8(wl, vals, k_scale, VS)
     assert err == 0
     compare(out, ref, "fp8-rising")
+
+
+def test_fp8_prepared_step_matches_the_oracle():
+    wl = W.config4()
+    vals_cpu = W.make_values_fp8(wl, poison_tails=True)
+    ref, kp, vp = oracle_step_fp8(wl, vals_cpu, KS, VS)
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
+    t = to_dev(wl, DEV)
+    ws = B.decode_workspace(wl.num_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                            wl.block_size, wl.max_seq_len, 0, device=DEV)
+    out = torch.full_like(vals["q"], float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    step = B.DecodeStep(out, vals["q"], vals["k_pool"], vals["v_pool"], t["block_tables"],
+                        t["seq_lens"], wl.scale, max_seq_len=wl.max_seq_len, workspace=ws,
+                        k_new=vals["k_new"], v_new=vals["v_new"],
+                        slot_mapping=t["slot_mapping"], pairs=t["pairs"], err_word=err,
+                        kv_scales=(KS, VS))
+    step.enqueue()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(vals["k_pool"].cpu().numpy(), kp)
+    assert np.array_equal(vals["v_pool"].cpu().numpy(), vp)
+    compare(out, ref, wl.name + "-fp8-prepared")
