@@ -991,7 +991,8 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
         dec_ms = statistics.median(per)
         achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
         timing = "CUDA events around each decode launch inside the timed steps, median"
-    traffic = recorded_traffic(name + ("-fp8" if fp8 is not None else ""))
+    traffic = recorded_traffic(name + ("-fp8" if fp8 is not None else "") +
+                               (f"-P{P_res}" if P_res > 0 else ""))
     kname = ("split_kernel<fp8> (pa_decode_fp8) + merge_kernel" if fp8 is not None else
              "split_kernel (pa_decode, balanced split) + merge_kernel" if P == 0 else
              "decode_kernel (pa_decode, fixed partitions) + merge_kernel")
