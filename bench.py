@@ -922,11 +922,20 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
                 partition_tokens=P, err_word=err,
                 kv_scales=(fp8, fp8) if fp8 is not None else None)
 
-    def e2e_body(j, k):
+    def e2e_body(j, k, sm_copies=True):
+        # the step's inputs in, the step, its output out: by the library's
+        # SM-driven pa_copy_host (one stream of kernels), or by the copy
+        # engine (torch copies)
         hb = host_pack[k]
-        stage[:hb.numel()].copy_(hb, non_blocking=True)
+        if sm_copies:
+            B.pa_copy_host(stage[:hb.numel()], hb)
+        else:
+            stage[:hb.numel()].copy_(hb, non_blocking=True)
         dsteps[(j, k)].enqueue()
-        host_out.copy_(outs[j], non_blocking=True)
+        if sm_copies:
+            B.pa_copy_host(host_out, outs[j])
+        else:
+            host_out.copy_(outs[j], non_blocking=True)
 
     def e2e_eager(i):
         e2e_body(*which(i))
@@ -939,19 +948,24 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
     try:
         e2e_graphs = {}
         cap2 = torch.cuda.Stream(dev)
-        for j in range(replicas):
-            for k in range(T):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap2):
-                    e2e_body(j, k)
-                e2e_graphs[(j, k)] = g
+        for sm_copies in (True, False):
+            for j in range(replicas):
+                for k in range(T):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=cap2):
+                        e2e_body(j, k, sm_copies)
+                    e2e_graphs[(j, k, sm_copies)] = g
         torch.cuda.synchronize()
-    except Exception as ex:  # capture of the host copies refused: eager only
+    except Exception as ex:  # capture refused: eager only
         e2e_graphs, graph_note = None, f"graph capture failed ({type(ex).__name__}: {ex})"
         torch.cuda.synchronize()
 
     def e2e_graphed(i):
-        e2e_graphs[which(i)].replay()
+        e2e_graphs[which(i) + (True,)].replay()
+        cur_stream.synchronize()
+
+    def e2e_graphed_ce(i):
+        e2e_graphs[which(i) + (False,)].replay()
         cur_stream.synchronize()
 
     def time_e2e(fn):
@@ -969,8 +983,10 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
                               world, sec) / 1e9, sec / e2e_steps
 
     eager_value, eager_s = time_e2e(e2e_eager)
+    ce_value = ce_s = None
     if e2e_graphs is not None:
         e2e_value, e2e_step_s = time_e2e(e2e_graphed)
+        ce_value, ce_s = time_e2e(e2e_graphed_ce)
     else:
         e2e_value, e2e_step_s = eager_value, eager_s
     h2d = sum(host_pack[which(i)[1]].numel() for i in range(e2e_steps)) / e2e_steps
@@ -1086,13 +1102,18 @@ def run_decode(args, env, cfg, bs, kv="bf16", partition_tokens=None, num_seqs=No
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": e2e_step_s * 1e3,
-                "launch": ("one CUDA graph replay per step (input copy, DecodeStep.enqueue: "
-                           "copy_blocks, reshape_and_cache, decode, merge; output copy), "
-                           "then a stream synchronise" if e2e_graphs is not None else
-                           graph_note),
+                "launch": ("one CUDA graph replay per step (pa_copy_host in, DecodeStep."
+                           "enqueue: copy_blocks, reshape_and_cache, decode, merge; "
+                           "pa_copy_host out), then a stream synchronise"
+                           if e2e_graphs is not None else graph_note),
+                "copy_engine": ({"value": ce_value, "ms_per_step": ce_s * 1e3,
+                                 "launch": "the same graph with the two copies done by the copy "
+                                           "engine (torch copies) instead of pa_copy_host"}
+                                if ce_value is not None else None),
                 "eager": {"value": eager_value, "ms_per_step": eager_s * 1e3,
                           "launch": "the same calls issued from Python every step "
-                                    "(DecodeStep.enqueue), then a stream synchronise"},
+                                    "(pa_copy_host, DecodeStep.enqueue, pa_copy_host), then a "
+                                    "stream synchronise"},
                 "note": "every step: its inputs (q, k, v of the new tokens, block tables, "
                         "lengths, slots, copy pairs) copied in from one page-locked buffer, "
                         "the public calls, the output copied out to page-locked memory, "

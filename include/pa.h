@@ -350,6 +350,25 @@ pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void
                          pa_stream_t stream);
 
 /*
+ * pa_copy_host — a byte copy between device memory of the current device and
+ * page-locked host memory (either side may be either), done by the SMs as a
+ * kernel on `stream`. The pages have no counterpart: it serves the
+ * end-to-end step, whose small inputs (the new tokens' q/k/v, tables,
+ * lengths, slots) and output cross the chip-to-chip link each step; as a
+ * kernel the copy joins the stream of the step's own kernels without a
+ * copy-engine hand-off between them.
+ *
+ * dst, src: 16-byte aligned, caller-owned, not overlapping; page-locked host
+ * memory must be mapped for the device (cudaHostAlloc / cudaHostRegister
+ * default flags on a unified-address system). nbytes: a multiple of 16
+ * (0 does nothing). Returns PA_ERR_INVALID_ARG for null or misaligned
+ * pointers, a size not a multiple of 16, or memory the device cannot address
+ * (pageable host memory, another device's memory); PA_ERR_CUDA on a launch
+ * failure. Asynchronous on `stream`, ordered after the work before it.
+ */
+pa_status pa_copy_host(void* dst, const void* src, size_t nbytes, pa_stream_t stream);
+
+/*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device
  * memory. The paper has no counterpart; this is a library convenience.
  *

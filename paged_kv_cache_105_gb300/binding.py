@@ -46,6 +46,7 @@ SIGNATURES = {
     "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                         C.c_float, _i, _vp, _vp]),
     "pa_swap_blocks": (_i, [_vp, _vp, _vp, _vp, _vp, _i, C.c_size_t, _i, _i, _vp, _vp]),
+    "pa_copy_host": (_i, [_vp, _vp, C.c_size_t, _vp]),
     "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
                            C.c_float, C.c_float, _i, _vp, C.c_size_t, _vp, _vp]),
 }
@@ -393,6 +394,26 @@ def pa_swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, err_word=None, stream=N
                               _ptr(err_word), _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_swap_blocks", st)
+
+
+def pa_copy_host(dst, src, *, stream=None):
+    """Copy src into dst (same byte size, contiguous) with the SMs, where
+    either tensor may be a CUDA tensor or page-locked host memory."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or page-locked (pinned) host memory")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("dst and src must hold the same number of bytes")
+    dev = dst.device if dst.is_cuda else (src.device if src.is_cuda else
+                                          torch.device("cuda", torch.cuda.current_device()))
+    st = lib().pa_copy_host(_ptr(dst), _ptr(src), n, _stream(stream, dev))
+    if st != PA_OK:
+        raise PAError("pa_copy_host", st)
 
 
 # ------------------------------------------------------------ prepared step

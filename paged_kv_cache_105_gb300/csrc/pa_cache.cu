@@ -24,7 +24,12 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
                          const int32_t* __restrict__ slot_mapping, int num_tokens,
                          int num_blocks, int n_kv, int chunks_per_row, int block_size,
                          int32_t* err) {
-  griddep_launch_dependents();  // a dependent decode may start launching now
+  // A programmatic dependent of the preceding kernel: wait for it (it may
+  // have produced the new K/V, the slots or a copied block), then let a
+  // dependent decode start launching; its prologue reads only inputs that
+  // were complete before this point.
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t per_tensor = (int64_t)num_tokens * n_kv * chunks_per_row;
   const int64_t total = 2 * per_tensor;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -56,6 +61,8 @@ __global__ void __launch_bounds__(256)
 copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                    const int32_t* __restrict__ pairs, int num_blocks, int64_t chunks_per_block,
                    int32_t* err) {
+  griddep_wait();  // a programmatic dependent: the preceding kernel first
+  griddep_launch_dependents();
   const int p = blockIdx.y;
   const int32_t src = __ldg(&pairs[2 * p]);
   const int32_t dst = __ldg(&pairs[2 * p + 1]);
@@ -83,6 +90,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restric
                              const int32_t* __restrict__ slot_mapping, int num_tokens,
                              int num_blocks, int n_kv, int chunks_per_row, int block_size,
                              float k_scale, float v_scale, int32_t* err) {
+  griddep_wait();  // as reshape_and_cache_kernel
   griddep_launch_dependents();
   const int64_t per_tensor = (int64_t)num_tokens * n_kv * chunks_per_row;
   const int64_t total = 2 * per_tensor;
@@ -149,6 +157,26 @@ swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
   }
 }
 
+// A plain copy of n16 16-byte chunks where either side may be page-locked
+// host memory the device addresses directly: the SMs move a step's small
+// inputs and outputs over the chip-to-chip link on the same stream as the
+// step's kernels, with no copy-engine hand-off between them.
+__global__ void __launch_bounds__(256)
+host_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
+  griddep_wait();  // a programmatic dependent: the preceding kernel first
+  griddep_launch_dependents();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {  // four loads in flight per thread
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+
 // The address through which the current device reaches `p`: device or
 // managed memory of this device as is, page-locked host memory through its
 // mapped device pointer. Anything else (pageable host memory, another
@@ -176,6 +204,25 @@ static bool device_view(const void* p, const void** out) {
     default:
       return false;
   }
+}
+
+// Launch as a programmatic dependent of the preceding kernel on `stream`:
+// the launch overlaps that kernel's tail, and the kernel waits for it
+// (griddep_wait) before touching memory.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 static bool supported_dims(int head_dim, int block_size) {
@@ -206,10 +253,10 @@ extern "C" pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
-      (const uint4*)k, (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping,
-      num_tokens, num_blocks, n_kv_heads, chunks, block_size, err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads),
+                             (cudaStream_t)stream, (const uint4*)k, (const uint4*)v,
+                             (uint4*)k_pool, (uint4*)v_pool, slot_mapping, num_tokens,
+                             num_blocks, n_kv_heads, chunks, block_size, err_word);
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_reshape_and_cache launch", e);
 }
 
@@ -227,9 +274,9 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* p
   int64_t bx = (2 * chunks + threads - 1) / threads;
   if (bx > 64) bx = 64;
   dim3 grid((unsigned)bx, (unsigned)n_pairs);
-  copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
-      (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), (cudaStream_t)stream,
+                             (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks,
+                             err_word);
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks launch", e);
 }
 
@@ -255,10 +302,11 @@ extern "C" pa_status pa_reshape_and_cache_fp8(const void* k, const void* v, void
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  reshape_and_cache_fp8_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
-      (const uint4*)k, (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping,
-      num_tokens, num_blocks, n_kv_heads, chunks, block_size, k_scale, v_scale, err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(reshape_and_cache_fp8_kernel, dim3((unsigned)blocks),
+                             dim3(threads), (cudaStream_t)stream, (const uint4*)k,
+                             (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping,
+                             num_tokens, num_blocks, n_kv_heads, chunks, block_size, k_scale,
+                             v_scale, err_word);
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_reshape_and_cache_fp8 launch", e);
 }
 
@@ -277,9 +325,9 @@ extern "C" pa_status pa_copy_blocks_fp8(void* k_pool, void* v_pool, const int32_
   int64_t bx = (2 * chunks + threads - 1) / threads;
   if (bx > 64) bx = 64;
   dim3 grid((unsigned)bx, (unsigned)n_pairs);
-  copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
-      (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks, err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), (cudaStream_t)stream,
+                             (uint4*)k_pool, (uint4*)v_pool, pairs, num_blocks, chunks,
+                             err_word);
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_blocks_fp8 launch", e);
 }
 
@@ -313,3 +361,21 @@ extern "C" pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k,
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_swap_blocks launch", e);
 }
+
+extern "C" pa_status pa_copy_host(void* dst, const void* src, size_t nbytes, pa_stream_t stream) {
+  if (nbytes == 0) return PA_OK;
+  if (!dst || !src || nbytes % 16 != 0) return PA_ERR_INVALID_ARG;
+  const void* dd;
+  const void* ds;
+  if (!device_view(dst, &dd) || !device_view(src, &ds)) return PA_ERR_INVALID_ARG;
+  if (!aligned16(dd) || !aligned16(ds)) return PA_ERR_INVALID_ARG;
+  const int64_t n16 = (int64_t)(nbytes / 16);
+  const int threads = 256;
+  int64_t blocks = (n16 + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * 2;
+  if (blocks > cap) blocks = cap;
+  cudaError_t e = launch_pdl(host_copy_kernel, dim3((unsigned)blocks), dim3(threads),
+                             (cudaStream_t)stream, (uint4*)dd, (const uint4*)ds, n16);
+  return e == cudaSuccess ? PA_OK : cuda_fail("pa_copy_host launch", e);
+}
+

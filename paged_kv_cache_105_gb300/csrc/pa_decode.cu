@@ -1328,6 +1328,7 @@ __device__ __forceinline__ void merge_row_coop(const MergeArgs& m, int row) {
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs m) {
   griddep_wait();  // the partials come from the decode grid
+  griddep_launch_dependents();  // a dependent (which waits for this grid) may launch
   if (m.coop) {  // grid = rows
     merge_row_coop<D>(m, blockIdx.x);
     return;

@@ -177,3 +177,8 @@ def test_prefill_and_swap_host_validation(L):
     assert s(p, p, p, p, p, -1, 1024, 4, 4, None, None) == INV
     assert s(None, None, None, None, None, 0, 1024, 4, 4, None, None) == B.PA_OK
     assert s(p, p, p, p, p, 1, 1024, 4, 4, None, None) == INV      # no device to address p
+    h = L.pa_copy_host
+    assert h(p, p, 0, None) == B.PA_OK                           # nothing to copy
+    assert h(None, p, 64, None) == INV
+    assert h(p, p, 24, None) == INV                              # not a 16-byte multiple
+    assert h(p, p, 64, None) == INV                              # no device to address p

@@ -82,3 +82,26 @@ def test_swap_refuses_pageable_host_memory():
         1024, 4, 4, None, C.c_void_p(torch.cuda.current_stream(DEV).cuda_stream))
     assert st == B.PA_ERR_INVALID_ARG
     assert np.all(pageable == 0)
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 819712, 3 << 20])
+def test_copy_host_both_ways_is_bit_exact(nbytes):
+    # pa_copy_host: pinned host -> device and back, checked against the bytes
+    g = torch.Generator().manual_seed(nbytes)
+    host = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8).pin_memory()
+    dev = torch.full((nbytes,), 7, dtype=torch.uint8, device=DEV)
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    B.pa_copy_host(dev, host)
+    B.pa_copy_host(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), host)
+    assert torch.equal(back, host)
+
+
+def test_copy_host_refuses_pageable_memory():
+    src = torch.zeros(64, dtype=torch.uint8)                    # pageable
+    dst = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(ValueError):
+        B.pa_copy_host(dst, src)
+    st = B.lib().pa_copy_host(dst.data_ptr(), src.data_ptr(), 64, None)
+    assert st == B.PA_ERR_INVALID_ARG
