@@ -8,7 +8,7 @@ import torch
 
 from oracle import paref
 from paged_kv_cache_105_gb300 import workloads as W
-from tests.helpers import bits, compare, gpu_step
+from tests.helpers import attention_threaded, bits, compare, gpu_step
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -44,11 +44,11 @@ def test_beam_steps_full_parity(keep):
     assert np.array_equal(bits(pools["v_pool"]), vp)
 
 
-def test_beam_search_full_size_sampled():
+def test_beam_search_full_size():
+    # every step's pool bytes; every output of three of the 32 steps
     ms = W.config6()
     base = W.make_values(ms.steps[0], device=DEV)
     kp, vp = bits(base["k_pool"]).copy(), bits(base["v_pool"]).copy()
-    rng = np.random.default_rng(6)
     for t, wl in enumerate(ms.steps):
         sv = W.make_step_values(wl, device=DEV)
         oracle_pools_step(wl, kp, vp, sv)
@@ -56,10 +56,9 @@ def test_beam_search_full_size_sampled():
         out, err = gpu_step(wl, vals)
         assert err == 0
         if t in (0, 13, len(ms.steps) - 1):
-            seqs = sorted(rng.choice(wl.num_seqs, 3, replace=False).tolist())
-            rows = np.array([(s, h) for s in seqs for h in range(wl.n_q_heads)], np.int32)
-            ref = paref.attention_paged(bits(sv["q"]), kp, vp, wl.block_tables, wl.seq_lens,
-                                        wl.scale, rows=rows)
-            compare(out[seqs].reshape(-1, wl.head_dim), ref, wl.name)
+            ref = attention_threaded(paref.attention_paged,
+                                     (bits(sv["q"]), kp, vp, wl.block_tables, wl.seq_lens,
+                                      wl.scale), wl.num_seqs, wl.n_q_heads, wl.head_dim)
+            compare(out, ref, wl.name)
     assert np.array_equal(bits(base["k_pool"]), kp)
     assert np.array_equal(bits(base["v_pool"]), vp)

@@ -111,7 +111,17 @@ def test_fp8_scales_apply():
     full_parity_fp8(wl, k_scale=0.25 * KS, v_scale=8.0 * VS)
 
 
-def test_fp8_long_context_full_size_sampled():
+def test_fp8_fragmented_mha_full_size_every_output():
+    wl = W.config3(block_size=16)
+    vals = W.make_values_fp8(wl, device=DEV, poison_tails=True)
+    seqs = list(range(wl.num_seqs))
+    ref = sampled_oracle(wl, vals, seqs, fp8_scales=(KS, VS))
+    out, err = gpu_step_fp8(wl, vals, KS, VS)
+    assert err == 0
+    compare(out[seqs], ref, wl.name + "-fp8")
+
+
+def test_fp8_long_context_full_size_every_output():
     wl = W.config5()
     vals = W.make_values_fp8(wl, device=DEV, poison_tails=True)
     seqs = list(range(wl.num_seqs))  # all 16 sequences, every head

@@ -1,7 +1,8 @@
 """GPU parity of chunked-prefill attention against the fp64 oracle: the
 chunk's K/V written by the cache write, then causal attention over the whole
-paged context. Same bar as decode: every bf16 output within 1e-2 of the
-oracle and every (token, head) row within 2e-2 relative L2 error."""
+paged context. Same bar as decode, element by element: |gpu - ref| <= 1e-2
+and |gpu - ref| / max(|ref|, 1e-2) <= 2e-2, and every (token, head) row
+within 2e-2 relative L2 error."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +38,22 @@ def oracle_prefill(wl, vals_cpu, rows=None):
     out = paref.prefill_paged(bits(vals_cpu["q"]), kp, vp, wl.block_tables, wl.seq_lens,
                               wl.cu_q, wl.scale, rows=rows)
     return out, kp, vp
+
+
+def oracle_prefill_threaded(wl, vals_cpu, rows):
+    """oracle_prefill's rows, split across host threads (independent rows)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    kp, vp = bits(vals_cpu["k_pool"]).copy(), bits(vals_cpu["v_pool"]).copy()
+    paref.reshape_and_cache(bits(vals_cpu["k_new"]), bits(vals_cpu["v_new"]), kp, vp,
+                            wl.slot_mapping)
+    q = bits(vals_cpu["q"])
+    chunks = [c for c in np.array_split(rows, max(1, min(32, os.cpu_count() or 1))) if len(c)]
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(lambda c: paref.prefill_paged(q, kp, vp, wl.block_tables,
+                                                          wl.seq_lens, wl.cu_q, wl.scale,
+                                                          rows=c), chunks))
+    return np.concatenate(parts, 0)
 
 
 CASES = [
@@ -83,13 +100,13 @@ def test_single_token_chunks_equal_decode():
 
 
 def test_chunked_prefill_full_size_sampled():
+    # every head of every 32nd chunk token and of the chunk edges: 9,472 rows
     wl = W.prefill_chunked()
     vals_cpu = W.make_prefill_values(wl)
-    rng = np.random.default_rng(0)
-    rows = np.stack([rng.integers(0, wl.total_q, 48), rng.integers(0, wl.n_q_heads, 48)],
-                    1).astype(np.int32)
-    rows[:8, 0] = [0, 1023, 1024, 4095, 4096, 7167, 7168, 8191]  # chunk edges
-    ref, _, _ = oracle_prefill(wl, vals_cpu, rows=rows)
+    toks = sorted(set(range(0, wl.total_q, 32)) |
+                  {1023, 1024, 4095, 4096, 7167, 7168, 8191, 1, 31, 33})
+    rows = np.array([(t, h) for t in toks for h in range(wl.n_q_heads)], np.int32)
+    ref = oracle_prefill_threaded(wl, vals_cpu, rows)
     vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
     out, err = gpu_prefill(wl, vals)
     assert err == 0
