@@ -45,8 +45,8 @@ def pytest_terminal_summary(terminalreporter):
                 cur[2], cur[4] = r, refv
             cur[3] = max(cur[3], row)
     tr = terminalreporter
-    tr.write_line("parity vs the fp64 oracle (bars: abs 1e-2, element rel 2e-2 with a "
-                  "1e-2 floor, row rel 2e-2)")
+    tr.write_line("parity vs the fp64 oracle (bars: abs 1e-2 or the bf16 rounding 2^-8|ref| "
+                  "where larger, element rel 2e-2 with a 1e-2 floor, row rel 2e-2)")
     for key in sorted(agg):
         n, a, r, row, refv = agg[key]
         tr.write_line(f"  {key:<40s} n={n:<9d} abs={a:.2e} rel={r:.2e} (ref {refv:+.2e}) "
