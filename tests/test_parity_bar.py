@@ -25,7 +25,7 @@ def test_one_step_off_above_four_fails():
     g = bf16(ref).float()
     g[0, 0, 2] += 2.0 ** -5  # one bf16 step at [4, 8)
     with pytest.raises(AssertionError):
-        compare(g.to(torch.bfloat16), ref, "step")
+        compare(g.to(torch.bfloat16), ref, "expected-fail: step")
 
 
 def test_near_zero_element_fails_the_relative_floor():
@@ -33,7 +33,7 @@ def test_near_zero_element_fails_the_relative_floor():
     g = bf16(ref).float()
     g[0, 0, 0] += 3e-4  # 3e-4 / max(1e-3, 1e-2) = 3e-2 > 2e-2
     with pytest.raises(AssertionError):
-        compare(g.to(torch.bfloat16), ref, "floor")
+        compare(g.to(torch.bfloat16), ref, "expected-fail: floor")
 
 
 def test_dropped_term_fails():
@@ -44,4 +44,4 @@ def test_dropped_term_fails():
     ref = (w[:, None] * v).sum(0)[None, None, :]
     wrong = ((w[:-1, None] * v[:-1]).sum(0) / w[:-1].sum())[None, None, :]
     with pytest.raises(AssertionError):
-        compare(bf16(wrong), ref, "dropped")
+        compare(bf16(wrong), ref, "expected-fail: dropped")
