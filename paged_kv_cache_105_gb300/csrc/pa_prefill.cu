@@ -370,7 +370,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       const uint32_t tS = tmem + tmem_s_col(wg, kt & 1);
       tc_ld32(tS + lane_off, sr[0]);
       tc_ld32(tS + lane_off + 32, sr[1]);
-      tc_wait_ld();
+      tc_wait_ld_bind(sr[0]);
+      tc_wait_ld_bind(sr[1]);
       const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
       const uint64_t vis = lim < 0 ? 0ull : tmask & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
@@ -429,7 +430,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t o[32];
             tc_ld32(tO + lane_off + cc, o);
-            tc_wait_ld();
+            tc_wait_ld_bind(o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tc_st32(tO + lane_off + cc, o);
@@ -471,7 +472,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
         tc_ld32(tO + lane_off + cc, o);
-        tc_wait_ld();
+        tc_wait_ld_bind(o);
         if (orow >= 0) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc);
 #pragma unroll
