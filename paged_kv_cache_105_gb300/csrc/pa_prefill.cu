@@ -418,14 +418,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       // P over S in TMEM: this thread's lane, hi then lo
       tc_st32(tS + lane_off, pk[0]);
       tc_st32(tS + lane_off + 32, pk[1]);
-      // O holds earlier tiles: rescale this warp's rows (alpha = 1 for the
-      // others) once P V(kt-1) is done. A warp waits here only when it
-      // rescales; P V(kt) cannot complete before this warp's P(kt) arrival,
-      // so the barrier is never two phases ahead of this wait.
-      if (kt > 0 && warp_need) {
+      // Wait for P V(kt-1) before this tile's P arrival. It was issued after
+      // the issuer waited for P(kt-1), so the P barrier cannot complete two
+      // phases (kt-1 and kt) before the issuer has seen the first: S(1) is
+      // issued up front, and without this wait a warpgroup could write P(0)
+      // and P(1) before its issuer looked. (P V(kt) cannot complete before
+      // this warp's P(kt) arrival, so this barrier is never two phases ahead
+      // of the wait either.) Then O holds earlier tiles only: rescale this
+      // warp's rows (alpha = 1 for the others) if the reference moved.
+      if (kt > 0) {
         wait(pv_bar, (kt - 1) & 1);
         tc_fence_after();
-        {
+        if (warp_need) {
 #pragma unroll
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t o[32];
