@@ -350,6 +350,23 @@ pa_status pa_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void
                          pa_stream_t stream);
 
 /*
+ * pa_check_bounded_wait — a check that the library's waits give up. The pages
+ * have no counterpart: it tests the failure behaviour of the kernels here.
+ *
+ * Every wait inside the library's kernels (on a copy landing, on tensor-core
+ * work, on another role's progress) is bounded: after a time limit (2 s in the
+ * kernels) it gives up, sets PA_DEV_ERR_TIMEOUT in the error word and lets the
+ * kernel finish, so a lost arrival cannot hang the GPU. This entry point runs
+ * the same bounded wait on a barrier that nothing arrives on, with the given
+ * limit (1 ns .. 2 s), in one thread on `stream`: afterwards *err_word has
+ * PA_DEV_ERR_TIMEOUT set and the context is usable.
+ *
+ * err_word: device int32 (required). Returns PA_ERR_INVALID_ARG for a null
+ * err_word or a limit outside (0, 2e9] ns; PA_ERR_CUDA on a launch failure.
+ */
+pa_status pa_check_bounded_wait(int32_t* err_word, int64_t limit_ns, pa_stream_t stream);
+
+/*
  * pa_copy_host — a byte copy between device memory of the current device and
  * page-locked host memory (either side may be either), done by the SMs as a
  * kernel on `stream`. The pages have no counterpart: it serves the

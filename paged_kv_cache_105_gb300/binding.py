@@ -47,6 +47,7 @@ SIGNATURES = {
                         C.c_float, _i, _vp, _vp]),
     "pa_swap_blocks": (_i, [_vp, _vp, _vp, _vp, _vp, _i, C.c_size_t, _i, _i, _vp, _vp]),
     "pa_copy_host": (_i, [_vp, _vp, C.c_size_t, _vp]),
+    "pa_check_bounded_wait": (_i, [_vp, C.c_int64, _vp]),
     "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, C.c_float,
                            C.c_float, C.c_float, _i, _vp, C.c_size_t, _vp, _vp]),
 }

@@ -1,9 +1,11 @@
-// Status strings, the thread-local CUDA error text and device queries.
+// Status strings, the thread-local CUDA error text, device queries, and the
+// check that the library's bounded waits give up.
 #include <cstdio>
 #include <mutex>
 #include <string>
 
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -46,3 +48,28 @@ extern "C" const char* pa_status_string(pa_status s) {
 }
 
 extern "C" const char* pa_last_cuda_error(void) { return pa::g_last_error.c_str(); }
+
+namespace pa {
+
+// One thread waits on an mbarrier that nothing arrives on, with the same
+// bounded wait the decode and prefill kernels use, and reports the timeout
+// through the error word: the wait gives up and the kernel returns.
+__global__ void bounded_wait_check_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbarrier_init();
+  if (!mbar_wait_bounded(b, 0, limit_ns)) report(err, PA_DEV_ERR_TIMEOUT);
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_check_bounded_wait(int32_t* err_word, int64_t limit_ns,
+                                           pa_stream_t stream) {
+  if (!err_word || limit_ns <= 0 || limit_ns > 2000000000LL) return PA_ERR_INVALID_ARG;
+  pa::bounded_wait_check_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(err_word,
+                                                                    (uint64_t)limit_ns);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : pa::cuda_fail("pa_check_bounded_wait launch", e);
+}
+

@@ -46,7 +46,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, giving up after
-// `limit_ns` nanoseconds of wall time. Returns false on timeout.
+// `limit_ns` nanoseconds of wall time, or after 2^28 polls should the timer
+// not advance. Returns false on giving up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
 #pragma unroll 1
@@ -54,10 +55,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
-  while (true) {
+  for (uint32_t i = 0; i < (1u << 28); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+  return false;
 }
 
 // Make mbarrier initialisation visible to the async (TMA) proxy.

@@ -182,3 +182,7 @@ def test_prefill_and_swap_host_validation(L):
     assert h(None, p, 64, None) == INV
     assert h(p, p, 24, None) == INV                              # not a 16-byte multiple
     assert h(p, p, 64, None) == INV                              # no device to address p
+    w = L.pa_check_bounded_wait
+    assert w(None, 1000, None) == INV                            # an error word is required
+    assert w(p, 0, None) == INV
+    assert w(p, 3_000_000_000, None) == INV                      # above the 2 s limit
