@@ -28,7 +28,9 @@
 //    next tile and P V of the previous one run on the tensor cores while the
 //    threads compute the softmax of the current one.
 //  * O is normalised and written as bf16 after the last tile.
-// Tiles are numbered so a sequence's latest (longest) tiles start first.
+// Blocks take the tiles longest first (longest_first_tile): the hardware
+// starts blocks in index order, so a list schedule that begins with the
+// costliest tiles ends near the average load per SM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -65,6 +67,7 @@ constexpr uint64_t kTWaitNs = 2000000000ull;      // 2 s: a wait that long is a 
 constexpr uint64_t kTWaitAfterFaultNs = 1000000ull;
 constexpr float kTLazyLog2 = 8.f;
 constexpr float kTLog2e = 1.4426950408889634f;
+constexpr int kTRankSeqs = 256;  // longest-first order for batches up to this many sequences
 
 struct PrefillArgs {
   __nv_bfloat16* out;
@@ -100,13 +103,117 @@ struct TCfg {
   static constexpr int NBARS = 4 * kTStages + 6 * kTWarpgroups;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
-  static constexpr size_t SMEM = 1024 + FAULT_OFF + 8;
+  static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g
+  static constexpr size_t SMEM = 1024 + SEL_OFF + 16;
 };
 
 // Byte offset of bf16 element (r, c) of a [rows][64] half-tile with the
 // 128-byte swizzle (8-row atoms of 1024 bytes; 16-byte chunks XOR row % 8).
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
+}
+
+// A tile is (sequence s, query tile qt, kv head g); its cost is the number of
+// 64-token K/V tiles it streams, plus one. The tile's last query position is
+// base_s + min((qt + 1) TQ, c_s) with base_s = L_s - c_s - 1, so the cost
+// never falls as qt grows, and cost >= T (T >= 2) holds exactly when
+// min((qt + 1) TQ, c_s) >= 64 (T - 2) - base_s. Returns the first such qt
+// below Q (the sequence's tile count), or Q.
+__device__ __forceinline__ int first_tile_at_least(long long T, int c, long long base, int Q,
+                                                   int TQ) {
+  if (T <= 1) return 0;
+  const long long R = (long long)kTKv * (T - 2) - base;
+  if (R > c) return Q;
+  if (R <= TQ) return 0;
+  const int q = (int)(R - 1) / TQ;  // ceil(R / TQ) - 1, with TQ < R <= c
+  return q < Q ? q : Q;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct TileSel {
+  int s, qt, g;  // s < 0: no tile for this block
+};
+
+// The tile of block `rank` in longest-first order: the rank-th costliest of
+// all tiles, ties in (s, qt, g) order. One warp; lane l holds sequences
+// l, l + 32, ... (at most kTRankSeqs). A binary search over the cost finds
+// the rank's cost class, then a scan over the sequences finds the tile.
+__device__ TileSel longest_first_tile(const PrefillArgs& a, int cap, long long rank, int lane) {
+  constexpr int J = kTRankSeqs / 32;
+  const int TQ = a.tile_tokens, S = a.num_seqs;
+  int cc[J], qq[J];
+  long long bb[J];
+  long long total = 0, tmax = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int s = lane + 32 * j;
+    cc[j] = 0;
+    qq[j] = 0;
+    bb[j] = 0;
+    if (s < S) {
+      const int c = __ldg(&a.cu_q[s + 1]) - __ldg(&a.cu_q[s]);
+      int L = __ldg(&a.seq_lens[s]);
+      if (L > cap) L = cap;
+      const int Q = c <= 0 ? 0 : min((c - 1) / TQ + 1, a.n_tiles);
+      cc[j] = c;
+      qq[j] = Q;
+      bb[j] = (long long)L - c - 1;
+      if (Q > 0) {
+        const long long pm = bb[j] + min((long long)Q * TQ, (long long)c);
+        tmax = max(tmax, 1 + (pm < 0 ? 0 : pm / kTKv + 1));
+        total += Q;
+      }
+    }
+  }
+  total = warp_sum_ll(total) * a.n_kv;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if (rank >= total) return {-1, 0, 0};
+  auto count_at_least = [&](long long T) {  // tiles of cost >= T
+    long long n = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      if (32 * j < S && qq[j] > 0) n += qq[j] - first_tile_at_least(T, cc[j], bb[j], qq[j], TQ);
+    return warp_sum_ll(n) * a.n_kv;
+  };
+  long long lo = 1, hi = tmax + 1;  // count_at_least(lo) > rank >= count_at_least(hi)
+#pragma unroll 1
+  while (hi - lo > 1) {
+    const long long mid = (lo + hi) >> 1;
+    if (count_at_least(mid) > rank) lo = mid;
+    else hi = mid;
+  }
+  long long r = rank - count_at_least(lo + 1);  // the rank among the tiles of cost lo
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (32 * j >= S) break;
+    int f0 = 0;
+    long long n = 0;
+    if (qq[j] > 0) {
+      f0 = first_tile_at_least(lo, cc[j], bb[j], qq[j], TQ);
+      n = (long long)(first_tile_at_least(lo + 1, cc[j], bb[j], qq[j], TQ) - f0) * a.n_kv;
+    }
+    long long inc = n;  // inclusive scan over the lanes, in sequence order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const long long here = __shfl_sync(0xffffffffu, inc, 31);
+    if (r < here) {
+      const int src = __ffs(__ballot_sync(0xffffffffu, r < inc)) - 1;
+      const long long idx = r - __shfl_sync(0xffffffffu, inc - n, src);
+      const int q0 = __shfl_sync(0xffffffffu, f0, src);
+      return {src + 32 * j, q0 + (int)(idx / a.n_kv), (int)(idx % a.n_kv)};
+    }
+    r -= here;
+  }
+  return {-1, 0, 0};  // not reached: the ranks below total cover every tile
 }
 
 // Roles: eight softmax warps (one row per thread); lane 0 of one warp issues
@@ -151,21 +258,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
-  const int s = blockIdx.y, g = blockIdx.z;
-  const int qt = a.n_tiles - 1 - (int)blockIdx.x;  // the latest tiles first
+  // ---- this block's tile: longest first; past kTRankSeqs sequences, the
+  // grid's own order (a sequence's latest tiles first)
+  const int cap = a.max_blocks * BS;
+  int s, qt, g;
+  if (a.num_seqs <= kTRankSeqs) {
+    int* sel = reinterpret_cast<int*>(smem + C::SEL_OFF);
+    if (warp == 0) {
+      const long long rank =
+          blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+      const TileSel t = longest_first_tile(a, cap, rank, lane);
+      if (lane == 0) {
+        sel[0] = t.s;
+        sel[1] = t.qt;
+        sel[2] = t.g;
+      }
+    }
+    __syncthreads();
+    s = sel[0];
+    qt = sel[1];
+    g = sel[2];
+    if (s < 0) return;
+  } else {
+    s = blockIdx.y;
+    g = blockIdx.z;
+    qt = a.n_tiles - 1 - (int)blockIdx.x;
+  }
   const int cq0 = __ldg(&a.cu_q[s]);
   const int c = __ldg(&a.cu_q[s + 1]) - cq0;
   const int G = a.group, TQ = a.tile_tokens;
   const int t0 = qt * TQ;
   // a chunk longer than max_q_len breaks the contract: flagged (rows beyond
   // the grid's n_tiles * TQ stay unwritten)
-  if (blockIdx.x == 0 && g == 0 && tid == 0 && c > a.max_q_len)
-    report(a.err, PA_DEV_ERR_SEQ_LEN);
+  if (qt == 0 && g == 0 && tid == 0 && c > a.max_q_len) report(a.err, PA_DEV_ERR_SEQ_LEN);
   if (c <= 0 || t0 >= c) return;
   int L = __ldg(&a.seq_lens[s]);
-  const int cap = a.max_blocks * BS;
   if (L > cap || L < c) {  // clamped / nothing visible: flagged, rows not written if L < c
-    if (tid == 0 && blockIdx.x == 0 && g == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
+    if (tid == 0 && qt == 0 && g == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
     if (L > cap) L = cap;
   }
   const int nt = min(TQ, c - t0);  // query tokens in this tile

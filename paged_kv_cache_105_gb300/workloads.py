@@ -455,6 +455,18 @@ def prefill_chunked(seed: int = 7) -> PrefillWorkload:
                          name="chunked-prefill-8x1024-ctx0to7168-bs16-q32kv8-d128")
 
 
+def prefill_mix(num_seqs: int, *, max_context: int = 200, max_chunk: int = 48,
+                seed: int = 0, **kw) -> PrefillWorkload:
+    """A mixed batch of many sequences: contexts uniform in [0, max_context),
+    chunks uniform in [0, max_chunk) (some empty), seeded; other arguments as
+    prefill_batch."""
+    rng = np.random.default_rng(seed * 7919 + num_seqs)
+    ctx = rng.integers(0, max_context, num_seqs)
+    ch = rng.integers(0, max_chunk, num_seqs)
+    kw.setdefault("name", f"prefill-mix-{num_seqs}seq")
+    return prefill_batch(ctx, ch, seed=seed, **kw)
+
+
 def make_prefill_values(wl: PrefillWorkload, device="cpu", seed=None):
     """bf16 N(0, 1): q and the chunk's new K/V [total_q, ...], the pools."""
     import torch

@@ -12,6 +12,7 @@ import torch
 
 from paged_kv_cache_105_gb300 import binding as B
 from paged_kv_cache_105_gb300 import workloads as W
+from oracle import paref
 from tests.helpers import bits, compare, gpu_step, oracle_step, sampled_oracle
 
 pytestmark = pytest.mark.gpu
@@ -295,3 +296,11 @@ def test_prepared_step_matches_the_oracle_eager_and_graphed():
     assert int(err.item()) == 0
     assert torch.equal(out.view(torch.int16), first.view(torch.int16))
     assert np.array_equal(bits(vals["k_pool"]), kp)
+    # a serving loop refreshes the step's inputs in place between replays:
+    # new queries, the same pools -> the oracle's attention over the new q
+    q2 = W.make_values(wl, seed=wl.seed + 1)["q"]
+    vals["q"].copy_(q2)
+    g.replay()
+    torch.cuda.synchronize()
+    ref2 = paref.attention_paged(bits(q2), kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+    compare(out, ref2, wl.name + "-prepared-new-q")

@@ -115,11 +115,33 @@ def test_chunked_prefill_full_size_sampled():
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("num_seqs", [255, 256, 257, 300])
+def test_many_sequences_every_row(num_seqs):
+    # Up to 256 sequences the blocks take the tiles longest first, beyond
+    # that in the grid's own order; either way every tile exactly once (the
+    # output starts as NaN, so a tile left out shows). Some chunks are empty.
+    wl = W.prefill_mix(num_seqs, Hq=12, Hkv=4, d=64, seed=11)
+    assert (wl.chunk_lens == 0).any()
+    vals_cpu = W.make_prefill_values(wl)
+    ref, kp, vp = oracle_prefill(wl, vals_cpu)
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
+    out, err = gpu_prefill(wl, vals)
+    assert err == 0
+    compare(out, ref, wl.name)
+
+
 def test_short_max_q_len_is_flagged():
-    wl = W.prefill_batch([10, 0], [40, 100], Hq=8, Hkv=8, d=64, seed=5)
-    vals = {k: v.to(DEV) for k, v in W.make_prefill_values(wl).items()}
+    wl = W.prefill_batch([10, 0], [40, 100], Hq=32, Hkv=8, d=64, seed=5)  # 64-token tiles
+    vals_cpu = W.make_prefill_values(wl)
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
     out, err = gpu_prefill(wl, vals, max_q_len=64)
     assert err & B.PA_DEV_ERR_SEQ_LEN
+    # the grid covers each chunk's first 64 tokens (max_q_len): those rows
+    # are still right, the second chunk's rows from 64 on stay unwritten
+    ref, _, _ = oracle_prefill(wl, vals_cpu)
+    keep = np.r_[0:40, 40:104]
+    compare(out[torch.from_numpy(keep).long()], ref[keep], wl.name + "-truncated")
+    assert torch.isnan(out[104:].float()).all()
 
 
 def test_bad_block_id_flagged():
