@@ -22,11 +22,11 @@
 //    every thread loads its row of S, masks it (causal, length, bad blocks),
 //    runs the online softmax in base 2 with a lazily moved reference
 //    (rescaling its row of O in TMEM in the rare case the reference moves),
-//    and writes P over its S in TMEM as a bf16 pair hi + lo; then
-//    O += P_hi V + P_lo V (M 128, N head_dim, A = P from TMEM, V read
-//    MN-major) accumulates in TMEM. S is double-buffered in TMEM: S of the
-//    next tile and P V of the previous one run on the tensor cores while the
-//    threads compute the softmax of the current one.
+//    and writes P to TMEM as a bf16 pair hi + lo; then O += P_hi V + P_lo V
+//    (M 128, N head_dim, A = P from TMEM, V read MN-major) accumulates in
+//    TMEM. S and P have TMEM buffers of their own: S of the next tile is
+//    computed as soon as the threads have loaded this one, and P V of the
+//    previous tile runs while they compute this softmax.
 //  * O is normalised and written as bf16 after the last tile.
 // Blocks take the tiles longest first (longest_first_tile): the hardware
 // starts blocks in index order, so a list schedule that begins with the
@@ -56,13 +56,12 @@ constexpr int kTTileRows = kTRows * kTWarpgroups;  // (token, head) rows per CTA
 constexpr int kTKv = 64;                    // K/V tokens per tile (N of S)
 constexpr int kTUnit = 16;                  // tokens per TMA unit
 constexpr int kTStages = 4;
-// TMEM columns: S of warpgroup w in buffer 0 at 64 w and in buffer 1 at
-// 384 + 64 w; its O at 128 + 128 w
+// TMEM columns of warpgroup w: O at 256 w (head_dim fp32 columns), S at
+// 256 w + 128 (64 fp32), P at 256 w + 192 (hi then lo: 32 + 32 bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 128;
-__host__ __device__ constexpr uint32_t tmem_s_col(int w, int b) {
-  return b ? 384 + 64 * w : 64 * w;
-}
+__host__ __device__ constexpr uint32_t tmem_o_col(int w) { return 256 * w; }
+__host__ __device__ constexpr uint32_t tmem_s_col(int w) { return 256 * w + 128; }
+__host__ __device__ constexpr uint32_t tmem_p_col(int w) { return 256 * w + 192; }
 constexpr uint64_t kTWaitNs = 2000000000ull;      // 2 s: a wait that long is a fault
 constexpr uint64_t kTWaitAfterFaultNs = 1000000ull;
 constexpr float kTLazyLog2 = 8.f;
@@ -97,10 +96,10 @@ struct TCfg {
   // S, well before its V is freed by its P V, so each streams on its own ring
   static constexpr int K_OFF = Q_OFF + kTWarpgroups * QWG;
   static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
-  // fullK, fullV, emptyK, emptyV (one per stage); per warpgroup: S done
-  // (one per TMEM buffer), P written, P V done, buffer free (one per buffer)
+  // fullK, fullV, emptyK, emptyV (one per stage); per warpgroup: S full,
+  // S free, P full, P V done; then the one-time start signal of warpgroup 1
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
-  static constexpr int NBARS = 4 * kTStages + 6 * kTWarpgroups;
+  static constexpr int NBARS = 4 * kTStages + 4 * kTWarpgroups + 1;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
   static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g
@@ -218,21 +217,22 @@ __device__ TileSel longest_first_tile(const PrefillArgs& a, int cap, long long r
 
 // Roles: eight softmax warps (one row per thread); lane 0 of one warp issues
 // the MMAs of warpgroup 0, of another those of warpgroup 1, of a third the
-// TMA copies (one warp scheduler each). Each warpgroup runs its own pipeline,
-// S(kt) -> softmax(kt) -> P V(kt) -> S(kt + 2), so the tensor cores work for
-// one warpgroup while the other computes its softmax; they share only the
-// K/V stages. The roles meet only at mbarriers, each arranged so that no
-// waiter can fall two phases behind:
-//   fullK/fullV[st]     copies landed               (loader -> both issuers)
-//   emptyK/emptyV[st]   S / P V of the tile done    (2 MMA commits -> loader)
+// TMA copies (one warp scheduler each). Each warpgroup runs its own pipeline:
+// the softmax of tile kt loads S(kt) and frees its buffer, so S(kt + 1) runs
+// on the tensor cores while the threads compute; P(kt) is stored once
+// P V(kt - 1) has read the P buffer. The warpgroups share only the K/V
+// stages. The roles meet only at mbarriers, each arranged so that no waiter
+// can fall two phases behind:
+//   fullK/fullV[st]   copies landed             (loader -> both issuers)
+//   emptyK/emptyV[st] S / P V of the tile done  (2 MMA commits -> loader)
 // and, per warpgroup w,
-//   s_bar[w][b]         S_w of the tile in buffer b (S commit -> softmax w)
-//   p_bar[w]            P_w of the tile written     (128 arrivals -> issuer w)
-//   pv_bar[w]           P V_w of the tile done      (P V commit -> softmax w)
-//   b_free[w][b]        P_w in buffer b consumed    (P V commit -> issuer w, softmax w)
-// P overwrites S in its TMEM buffer (hi in the first 32 columns, lo in the
-// next 32, bf16 pairs) and the P V MMA reads it from there, so the softmax of
-// the next tile never waits for this P V except to rescale O.
+//   s_full[w]         S_w(kt) in TMEM           (S commit -> softmax w)
+//   s_free[w]         S_w(kt) loaded            (128 arrivals -> issuer w)
+//   p_full[w]         P_w(kt) in TMEM           (128 arrivals -> issuer w)
+//   pv_done[w]        P V_w(kt) done            (P V commit -> softmax w)
+// S(kt + 1) is issued after s_free(kt), which follows s_full(kt); P V(kt)
+// after p_full(kt), and P(kt + 1) is stored after pv_done(kt): each barrier
+// completes a phase only after its waiter has seen the one before.
 template <int D, int BS>
 __global__ void __launch_bounds__(kTCtaThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -251,10 +251,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   const int wg = (tid >> 7) & 1, lr = tid & 127;  // warpgroup; row within it = TMEM lane
   const uint32_t fullK = sbase + C::BAR_OFF, fullV = fullK + 8 * kTStages;
   const uint32_t emptyK = fullV + 8 * kTStages, emptyV = emptyK + 8 * kTStages;
-  // per warpgroup w: s_bar[w][b] at s_bar0 + 16 w + 8 b, p_bar[w] at
-  // p_bar0 + 8 w, pv_bar[w] at pv_bar0 + 8 w, b_free[w][b] at b_free0 + 16 w + 8 b
-  const uint32_t s_bar0 = emptyV + 8 * kTStages, p_bar0 = s_bar0 + 16 * kTWarpgroups;
-  const uint32_t pv_bar0 = p_bar0 + 8 * kTWarpgroups, b_free0 = pv_bar0 + 8 * kTWarpgroups;
+  // per warpgroup w, 8 bytes each: s_full, s_free, p_full, pv_done at
+  // s_full0 + 32 w + 0, 8, 16, 24
+  const uint32_t s_full0 = emptyV + 8 * kTStages;
+  const uint32_t go1 = s_full0 + 32 * kTWarpgroups;
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -326,8 +326,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       mbar_init(emptyK + 8 * st, kTWarpgroups);
       mbar_init(emptyV + 8 * st, kTWarpgroups);
     }
-    for (int w = 0; w < kTWarpgroups; ++w)
-      mbar_init(p_bar0 + 8 * w, 128);  // every thread of warpgroup w, once per tile
+    for (int w = 0; w < kTWarpgroups; ++w) {  // every thread of warpgroup w, once per tile
+      mbar_init(s_full0 + 32 * w + 8, 128);
+      mbar_init(s_full0 + 32 * w + 16, 128);
+    }
 
     *fault = 0;
     fence_mbarrier_init();
@@ -339,6 +341,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   const uint32_t tmem = *tmem_slot;
 
   auto wait = [&](uint32_t bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return;
     const uint64_t limit = *fault ? kTWaitAfterFaultNs : kTWaitNs;
     if (!mbar_wait_bounded(bar, parity, limit)) {
       report(a.err, PA_DEV_ERR_TIMEOUT);
@@ -366,58 +369,58 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   };
 
   if (warp == kTLoadWarp) {
-    // ---- copies: K and V of every tile through their rings
+    // ---- copies: K and V of every tile through their rings. Lane j below
+    // NB * KH issues box j (block j / KH, 64-column half j % KH) of each
+    // tile, so one warp instruction starts a tile's copies; the block ids of
+    // the next tile are loaded while this one is copied.
+    constexpr int NBOX = NB * C::KH;
+    static_assert(NBOX <= 32, "one box per lane");
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
+    }
+    const int bi = lane / C::KH, bh = lane % C::KH;  // this lane's box: block, half
+    auto box_id = [&](int kt) {
+      const int tok = kt * kTKv + bi * C::ROWS;
+      return (lane < NBOX && tok < L) ? __ldg(&table[tok / BS]) : -1;
+    };
+    int id_nxt = n_kv > 0 ? box_id(0) : -1;
 #pragma unroll 1
-      for (int kt = 0; kt < n_kv; ++kt) {
-        const int st = kt % kTStages;
-        int ids[NB];
-        tile_ids(kt, ids);
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int tok = kt * kTKv + i * C::ROWS;
-          if (tok >= L) continue;
-          if (ids[i] >= 0 && ids[i] < a.num_blocks) bytes += C::KH * C::ROWS * 128;
-          else report(a.err, PA_DEV_ERR_BLOCK_ID);
+    for (int kt = 0; kt < n_kv; ++kt) {
+      const int st = kt % kTStages;
+      const int id = id_nxt;
+      if (kt + 1 < n_kv) id_nxt = box_id(kt + 1);
+      const int tok = kt * kTKv + bi * C::ROWS;
+      const bool present = lane < NBOX && tok < L;
+      const bool ok = present && id >= 0 && id < a.num_blocks;
+      if (present && !ok && bh == 0) report(a.err, PA_DEV_ERR_BLOCK_ID);
+      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, ok)) * C::ROWS * 128;
+      const int32_t y = (id * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
+#pragma unroll 1
+      for (int kv = 0; kv < 2; ++kv) {
+        if (kt >= kTStages)  // the stage's previous tile is done with it
+          wait((kv ? emptyV : emptyK) + 8 * st, ((kt - kTStages) / kTStages) & 1);
+        const uint32_t fb = (kv ? fullV : fullK) + 8 * st;
+        if (lane == 0) {
+          if (bytes == 0) mbar_arrive(fb);
+          else mbar_arrive_expect_tx(fb, bytes);
         }
-        for (int kv = 0; kv < 2; ++kv) {
-          if (kt >= kTStages)  // the stage's previous tile is done with it
-            wait((kv ? emptyV : emptyK) + 8 * st, ((kt - kTStages) / kTStages) & 1);
-          const uint32_t fb = (kv ? fullV : fullK) + 8 * st;
-          if (bytes == 0) {
-            mbar_arrive(fb);
-            continue;
-          }
-          mbar_arrive_expect_tx(fb, bytes);
+        __syncwarp();
+        if (ok) {
           const uint32_t dst = sbase + (kv ? C::V_OFF : C::K_OFF) + st * C::KV_BYTES;
-#pragma unroll
-          for (int i = 0; i < NB; ++i) {
-            const int tok = kt * kTKv + i * C::ROWS;
-            if (tok >= L || ids[i] < 0 || ids[i] >= a.num_blocks) continue;
-            const int32_t y = (ids[i] * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
-#pragma unroll
-            for (int h = 0; h < C::KH; ++h)
-              tma_load_2d(dst + h * C::HALF + i * C::ROWS * 128, kv ? &tmv : &tmk, h * 64, y,
-                          fb);
-          }
+          tma_load_2d(dst + bh * C::HALF + bi * C::ROWS * 128, kv ? &tmv : &tmk, bh * 64, y, fb);
         }
       }
     }
     __syncwarp();
   } else if (warp == kTIssue0Warp || warp == kTIssue1Warp) {
-    // ---- the MMAs of warpgroup w, issued by one lane:
-    // S_w(0), S_w(1), then per tile P V_w(kt) and S_w(kt + 2).
-    // S_w(kt) = Q_w K(kt)^T goes into buffer kt & 1 of the warpgroup's S
-    // (double-buffered, so S_w(kt+1) is ready when the softmax of kt ends);
-    // O_w += P_hi V + P_lo V once the softmax has written P_w(kt) over S_w(kt).
-    // Operand descriptors: the start address sits in the low 14 bits in
-    // 16-byte units (shared addresses stay below 2^18), so an offset into a
+    // ---- the MMAs of warpgroup w, issued by one lane: S_w(0), then per
+    // tile S_w(kt + 1) (once the softmax has loaded S_w(kt)) and P V_w(kt)
+    // (once it has stored P_w(kt)). S_w(kt) = Q_w K(kt)^T; O_w += P_hi V +
+    // P_lo V. Operand descriptors: the start address sits in the low 14 bits
+    // in 16-byte units (shared addresses stay below 2^18), so an offset into a
     // tile is added to the descriptor directly; they are formed before the
-    // waits, so that each MMA issues on its own (the issuing lane shares its
-    // scheduler with two softmax warps).
+    // waits, so that each MMA issues on its own.
     const int w = warp == kTIssue0Warp ? 0 : 1;
     if (lane == 0) {
       const uint64_t dq = tc_desc_sw128(sbase + C::Q_OFF + w * C::QWG, 16, 1024);
@@ -425,25 +428,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       const uint64_t dv = tc_desc_sw128(sbase + C::V_OFF, C::HALF, 1024);
       constexpr uint32_t kIdS = tc_idesc_bf16(kTRows, kTKv, 0);
       constexpr uint32_t kIdPV = tc_idesc_bf16(kTRows, D, 1);
-      const uint32_t s_bar = s_bar0 + 16 * w, b_free = b_free0 + 16 * w;
+      const uint32_t s_full = s_full0 + 32 * w, s_free = s_full + 8;
+      const uint32_t p_full = s_full + 16, pv_done = s_full + 24;
+      const uint32_t tS = tmem + tmem_s_col(w), tP = tmem + tmem_p_col(w);
+      const uint32_t tO = tmem + tmem_o_col(w);
       uint64_t dqs[D / 16];
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         dqs[ks] = dq + (((ks >> 2) * C::QHALF + (ks & 3) * 32) >> 4);
       auto issue_s = [&](int kt) {
-        const int st = kt % kTStages, buf = kt & 1;
+        const int st = kt % kTStages;
         uint64_t dks[D / 16];
         const uint64_t dk_st = dk + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           dks[ks] = dk_st + (((ks >> 2) * C::HALF + (ks & 3) * 32) >> 4);
-        const uint32_t d = tmem + tmem_s_col(w, buf);
-        if (kt >= 2) wait(b_free + 8 * buf, ((kt - 2) >> 1) & 1);  // P V_w(kt-2) done
+        if (kt >= 1) wait(s_free, (kt - 1) & 1);  // the softmax has loaded S_w(kt - 1)
         wait(fullK + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(d, dqs[ks], dks[ks], kIdS, ks > 0);
-        tc_commit(s_bar + 8 * buf);
+        for (int ks = 0; ks < D / 16; ++ks) tc_mma_bf16(tS, dqs[ks], dks[ks], kIdS, ks > 0);
+        tc_commit(s_full);
         tc_commit(emptyK + 8 * st);
       };
       auto issue_pv = [&](int kt) {
@@ -452,35 +457,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
         const uint64_t dv_st = dv + ((st * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kTKv / 16; ++ks) dvs[ks] = dv_st + ks * 128;
-        const uint32_t a = tmem + tmem_s_col(w, kt & 1), o = tmem + kTmemO + w * 128;
         const uint32_t first = kt == 0;
-        wait(p_bar0 + 8 * w, kt & 1);  // P_w(kt) written (and P V_w(kt-1) seen complete)
+        wait(p_full, kt & 1);  // P_w(kt) stored (after P V_w(kt - 1) was done)
         wait(fullV + 8 * st, (kt / kTStages) & 1);
         tc_fence_after();
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < kTKv / 16; ++ks)
-            tc_mma_bf16_ta64(o, a + part * 32 + ks * 8, dvs[ks], kIdPV,
+            tc_mma_bf16_ta64(tO, tP + part * 32 + ks * 8, dvs[ks], kIdPV,
                              (part | ks) ? 1u : !first);
-        tc_commit(pv_bar0 + 8 * w);
+        tc_commit(pv_done);
         tc_commit(emptyV + 8 * st);
-        tc_commit(b_free + 8 * (kt & 1));
       };
+      // Warpgroup 1 starts once S_0(0) is done, so that the two warpgroups
+      // run out of phase to begin with.
+      if (w == 1 && n_kv > 0) wait(go1, 0);
       if (n_kv > 0) issue_s(0);
-      if (n_kv > 1) issue_s(1);
+      if (w == 0 && n_kv > 0) tc_commit(go1);  // used once: one phase
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
+        if (kt + 1 < n_kv) issue_s(kt + 1);
         issue_pv(kt);
-        if (kt + 2 < n_kv) issue_s(kt + 2);
       }
     }
     __syncwarp();
   } else {
     // ---- the softmax warps: one row per thread, on warpgroup wg's barriers
-    const uint32_t tO = tmem + kTmemO + wg * 128;
-    const uint32_t s_bar = s_bar0 + 16 * wg, p_bar = p_bar0 + 8 * wg;
-    const uint32_t pv_bar = pv_bar0 + 8 * wg, b_free = b_free0 + 16 * wg;
+    const uint32_t tO = tmem + tmem_o_col(wg), tS = tmem + tmem_s_col(wg);
+    const uint32_t tP = tmem + tmem_p_col(wg);
+    const uint32_t s_full = s_full0 + 32 * wg, s_free = s_full + 8;
+    const uint32_t p_full = s_full + 16, pv_done = s_full + 24;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float m = -INFINITY, l = 0.f;
     int ids_nxt[NB];
@@ -490,17 +497,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       const int st = kt % kTStages;
       const uint64_t tmask = tile_mask(kt, ids_nxt);
       if (kt + 1 < n_kv) tile_ids(kt + 1, ids_nxt);  // in flight during this tile
-      wait(s_bar + 8 * (kt & 1), (kt >> 1) & 1);  // S(kt) is in TMEM
+      wait(s_full, kt & 1);  // S(kt) is in TMEM
       tc_fence_after();
       // masked, lazy online softmax of this thread's row. Scores stay in raw
       // units (the scale, > 0, goes into one FFMA per weight); masked
       // positions become -inf. On tiles the row sees whole, nothing is masked.
       uint32_t sr[2][32];
-      const uint32_t tS = tmem + tmem_s_col(wg, kt & 1);
       tc_ld32(tS + lane_off, sr[0]);
       tc_ld32(tS + lane_off + 32, sr[1]);
       tc_wait_ld_bind(sr[0]);
       tc_wait_ld_bind(sr[1]);
+      tc_fence_before();
+      mbar_arrive(s_free);  // the S buffer may take the next tile
       const int lim = min(kTKv - 1, pos - kt * kTKv);  // last position this row may see
       const uint64_t vis = lim < 0 ? 0ull : tmask & (lim >= 63 ? ~0ull : ((2ull << lim) - 1));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
@@ -544,19 +552,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                                p1 - __uint_as_float(pk[0][k] & 0xffff0000u));
       }
       l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-      // P over S in TMEM: this thread's lane, hi then lo
-      tc_st32(tS + lane_off, pk[0]);
-      tc_st32(tS + lane_off + 32, pk[1]);
-      // Wait for P V(kt-1) before this tile's P arrival. It was issued after
-      // the issuer waited for P(kt-1), so the P barrier cannot complete two
-      // phases (kt-1 and kt) before the issuer has seen the first: S(1) is
-      // issued up front, and without this wait a warpgroup could write P(0)
-      // and P(1) before its issuer looked. (P V(kt) cannot complete before
-      // this warp's P(kt) arrival, so this barrier is never two phases ahead
-      // of the wait either.) Then O holds earlier tiles only: rescale this
-      // warp's rows (alpha = 1 for the others) if the reference moved.
+      // P(kt) goes to the P buffer once P V(kt - 1) has read it. O then holds
+      // earlier tiles only: rescale this warp's rows (alpha = 1 for the
+      // others) if the reference moved.
       if (kt > 0) {
-        wait(pv_bar, (kt - 1) & 1);
+        wait(pv_done, (kt - 1) & 1);
         tc_fence_after();
         if (warp_need) {
 #pragma unroll
@@ -568,9 +568,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tc_st32(tO + lane_off + cc, o);
           }
-          tc_wait_st();
         }
       }
+      tc_st32(tP + lane_off, pk[0]);  // this thread's lane, hi then lo
+      tc_st32(tP + lane_off + 32, pk[1]);
       tc_wait_st();
       if (tmask != ~0ull) {
         // V rows with no token of the sequence may hold anything (even NaN):
@@ -589,16 +590,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       }
       if (tmask != ~0ull) fence_proxy_async_smem();  // zeroed rows before the MMA reads them
       tc_fence_before();
-      mbar_arrive(p_bar);
+      mbar_arrive(p_full);
     }
 
     // ---- normalise and write the rows
     if (n_kv > 0) {
-      // The last P V (and with it every earlier one). Waited on its own
-      // buffer-free barrier: P V(n-2) may still be running, so pv_bar could be
-      // two phases behind this wait, while b_free[(n-1) & 1] has seen
-      // P V(n-3) (S(n-1) waited for it) and has no later phase.
-      wait(b_free + 8 * ((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1);
+      // The last P V (and with it every earlier one): the phase after the
+      // one this thread saw before storing P(n - 1).
+      wait(pv_done, (n_kv - 1) & 1);
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
