@@ -374,7 +374,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     // tile, so one warp instruction starts a tile's copies; the block ids of
     // the next tile are loaded while this one is copied.
     constexpr int NBOX = NB * C::KH;
-    static_assert(NBOX <= 32, "one box per lane");
+    static_assert(2 * NBOX <= 32, "one box per lane");
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
@@ -396,19 +396,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       if (present && !ok && bh == 0) report(a.err, PA_DEV_ERR_BLOCK_ID);
       const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, ok)) * C::ROWS * 128;
       const int32_t y = (id * a.n_kv + g) * BS + (BS > kTUnit ? tok % BS : 0);
-#pragma unroll 1
-      for (int kv = 0; kv < 2; ++kv) {
-        if (kt >= kTStages)  // the stage's previous tile is done with it
-          wait((kv ? emptyV : emptyK) + 8 * st, ((kt - kTStages) / kTStages) & 1);
-        const uint32_t fb = (kv ? fullV : fullK) + 8 * st;
-        if (lane == 0) {
-          if (bytes == 0) mbar_arrive(fb);
-          else mbar_arrive_expect_tx(fb, bytes);
+      if (kt >= kTStages) {  // the stages' previous tile is done with them
+        wait(emptyK + 8 * st, ((kt - kTStages) / kTStages) & 1);
+        wait(emptyV + 8 * st, ((kt - kTStages) / kTStages) & 1);
+      }
+      if (lane == 0) {
+        if (bytes == 0) {
+          mbar_arrive(fullK + 8 * st);
+          mbar_arrive(fullV + 8 * st);
+        } else {
+          mbar_arrive_expect_tx(fullK + 8 * st, bytes);
+          mbar_arrive_expect_tx(fullV + 8 * st, bytes);
         }
-        __syncwarp();
-        if (ok) {
-          const uint32_t dst = sbase + (kv ? C::V_OFF : C::K_OFF) + st * C::KV_BYTES;
-          tma_load_2d(dst + bh * C::HALF + bi * C::ROWS * 128, kv ? &tmv : &tmk, bh * 64, y, fb);
+      }
+      __syncwarp();
+      // lanes 0 .. NBOX-1 copy K, lanes NBOX .. 2 NBOX-1 the same boxes of V
+      {
+        const int src = lane < NBOX ? lane : lane - NBOX;  // box index
+        const int okb = __shfl_sync(0xffffffffu, (int)ok, src & 31);
+        const int yb = __shfl_sync(0xffffffffu, y, src & 31);
+        const bool isv = lane >= NBOX;
+        if (lane < 2 * NBOX && okb) {
+          const int b_i = src / C::KH, b_h = src % C::KH;
+          const uint32_t dst = sbase + (isv ? C::V_OFF : C::K_OFF) + st * C::KV_BYTES +
+                               b_h * C::HALF + b_i * C::ROWS * 128;
+          tma_load_2d(dst, isv ? &tmv : &tmk, b_h * 64, yb, (isv ? fullV : fullK) + 8 * st);
         }
       }
     }
