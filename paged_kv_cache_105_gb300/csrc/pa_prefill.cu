@@ -77,6 +77,7 @@ struct PrefillArgs {
   int32_t* err;
   int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
   int tile_tokens;  // query tokens per tile: 256 / G, rounded down
+  int rank_tiles;   // 1: blocks take the tiles longest first (longest_first_tile)
   int n_tiles;      // grid.x: tiles of the longest chunk
   int max_q_len;    // host bound of the chunk lengths
   float scale_log2;
@@ -102,8 +103,9 @@ struct TCfg {
   static constexpr int NBARS = 4 * kTStages + 4 * kTWarpgroups + 1;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
-  static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g
-  static constexpr size_t SMEM = 1024 + SEL_OFF + 16;
+  static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g, cq0, c, L
+  static constexpr int ROWS_OFF = SEL_OFF + 24;  // its first output row
+  static constexpr size_t SMEM = 1024 + ROWS_OFF + 16;
 };
 
 // Byte offset of bf16 element (r, c) of a [rows][64] half-tile with the
@@ -118,8 +120,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // never falls as qt grows, and cost >= T (T >= 2) holds exactly when
 // min((qt + 1) TQ, c_s) >= 64 (T - 2) - base_s. Returns the first such qt
 // below Q (the sequence's tile count), or Q.
-__device__ __forceinline__ int first_tile_at_least(long long T, int c, long long base, int Q,
-                                                   int TQ) {
+__device__ __forceinline__ int first_tile_at_least(int T, int c, int base, int Q, int TQ) {
   if (T <= 1) return 0;
   const long long R = (long long)kTKv * (T - 2) - base;
   if (R > c) return Q;
@@ -128,26 +129,27 @@ __device__ __forceinline__ int first_tile_at_least(long long T, int c, long long
   return q < Q ? q : Q;
 }
 
-__device__ __forceinline__ long long warp_sum_ll(long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 struct TileSel {
   int s, qt, g;  // s < 0: no tile for this block
+  int cq0, c, L;  // its sequence's cu_q entry, chunk length, seq_lens entry (cq0 -1: not read)
 };
 
-// The tile of block `rank` in longest-first order: the rank-th costliest of
-// all tiles, ties in (s, qt, g) order. One warp; lane l holds sequences
-// l, l + 32, ... (at most kTRankSeqs). A binary search over the cost finds
-// the rank's cost class, then a scan over the sequences finds the tile.
+// The tile of block `rank` in longest-first order. The kv heads of a
+// (sequence, query tile) pair cost the same, so the order is that of the
+// pairs, costliest first with ties in (s, qt) order, each pair repeated for
+// g = 0 .. n_kv - 1: block `rank` takes pair rank / n_kv, head rank % n_kv.
+// One warp; lane l holds sequences l, l + 32, ... (at most kTRankSeqs, and
+// the host keeps the pair count below 2^31). A search over the cost finds
+// the pair's cost class: up to 32 sequences, each lane tries its own cost
+// and sums over every sequence (a 32-way split per round); beyond, a binary
+// search with one warp reduction per step. Then a scan over the sequences
+// finds the pair.
 __device__ TileSel longest_first_tile(const PrefillArgs& a, int cap, long long rank, int lane) {
   constexpr int J = kTRankSeqs / 32;
   const int TQ = a.tile_tokens, S = a.num_seqs;
-  int cc[J], qq[J];
-  long long bb[J];
-  long long total = 0, tmax = 0;
+  int cc[J], qq[J], bb[J];
+  int c00 = 0, l00 = 0;  // cu_q and seq_lens of sequence `lane`
+  int pairs = 0, tmax = 0;
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     const int s = lane + 32 * j;
@@ -155,64 +157,93 @@ __device__ TileSel longest_first_tile(const PrefillArgs& a, int cap, long long r
     qq[j] = 0;
     bb[j] = 0;
     if (s < S) {
-      const int c = __ldg(&a.cu_q[s + 1]) - __ldg(&a.cu_q[s]);
-      int L = __ldg(&a.seq_lens[s]);
-      if (L > cap) L = cap;
+      const int q0 = __ldg(&a.cu_q[s]), lr = __ldg(&a.seq_lens[s]);
+      if (j == 0) {
+        c00 = q0;
+        l00 = lr;
+      }
+      const int c = __ldg(&a.cu_q[s + 1]) - q0;
+      // L outside [0, cap] costs as its clamp does: nothing is visible
+      // below 0, and the kernel clamps above cap
+      const int L = min(max(lr, 0), cap);
       const int Q = c <= 0 ? 0 : min((c - 1) / TQ + 1, a.n_tiles);
       cc[j] = c;
       qq[j] = Q;
-      bb[j] = (long long)L - c - 1;
+      bb[j] = L - c - 1;
       if (Q > 0) {
-        const long long pm = bb[j] + min((long long)Q * TQ, (long long)c);
-        tmax = max(tmax, 1 + (pm < 0 ? 0 : pm / kTKv + 1));
-        total += Q;
+        const long long pm = (long long)bb[j] + min((long long)Q * TQ, (long long)c);
+        tmax = max(tmax, (int)(1 + (pm < 0 ? 0 : pm / kTKv + 1)));
+        pairs += Q;
       }
     }
   }
-  total = warp_sum_ll(total) * a.n_kv;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  if (rank >= total) return {-1, 0, 0};
-  auto count_at_least = [&](long long T) {  // tiles of cost >= T
-    long long n = 0;
+  pairs = __reduce_add_sync(0xffffffffu, pairs);
+  tmax = __reduce_max_sync(0xffffffffu, tmax);
+  if (rank >= (long long)pairs * a.n_kv) return {-1, 0, 0, 0, 0, 0};
+  const int pr = (int)(rank / a.n_kv), g = (int)(rank % a.n_kv);
+  auto count_at_least = [&](int T) {  // pairs of cost >= T
+    int n = 0;
 #pragma unroll
     for (int j = 0; j < J; ++j)
       if (32 * j < S && qq[j] > 0) n += qq[j] - first_tile_at_least(T, cc[j], bb[j], qq[j], TQ);
-    return warp_sum_ll(n) * a.n_kv;
+    return (int)__reduce_add_sync(0xffffffffu, n);
   };
-  long long lo = 1, hi = tmax + 1;  // count_at_least(lo) > rank >= count_at_least(hi)
+  int lo = 1, hi = tmax + 1;  // count_at_least(lo) > pr >= count_at_least(hi)
+  if (S <= 32) {
 #pragma unroll 1
-  while (hi - lo > 1) {
-    const long long mid = (lo + hi) >> 1;
-    if (count_at_least(mid) > rank) lo = mid;
-    else hi = mid;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) >> 5;
+      const int T = lo + lane * step;
+      int n = 0;
+#pragma unroll 1
+      for (int q = 0; q < S; ++q) {  // sequence q, from lane q
+        const int cq = __shfl_sync(0xffffffffu, cc[0], q);
+        const int nq = __shfl_sync(0xffffffffu, qq[0], q);
+        const int bq = __shfl_sync(0xffffffffu, bb[0], q);
+        if (nq > 0) n += nq - first_tile_at_least(T, cq, bq, nq, TQ);
+      }
+      // lanes below the first count <= pr: lane 0 (T = lo) always counts > pr
+      const unsigned more = __ballot_sync(0xffffffffu, T < hi && n > pr);
+      lo += (31 - __clz(more)) * step;
+      hi = min(hi, lo + step);
+    }
+  } else {
+#pragma unroll 1
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (count_at_least(mid) > pr) lo = mid;
+      else hi = mid;
+    }
   }
-  long long r = rank - count_at_least(lo + 1);  // the rank among the tiles of cost lo
+  int r = pr - count_at_least(lo + 1);  // the rank among the pairs of cost lo
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     if (32 * j >= S) break;
-    int f0 = 0;
-    long long n = 0;
+    int f0 = 0, n = 0;
     if (qq[j] > 0) {
       f0 = first_tile_at_least(lo, cc[j], bb[j], qq[j], TQ);
-      n = (long long)(first_tile_at_least(lo + 1, cc[j], bb[j], qq[j], TQ) - f0) * a.n_kv;
+      n = first_tile_at_least(lo + 1, cc[j], bb[j], qq[j], TQ) - f0;
     }
-    long long inc = n;  // inclusive scan over the lanes, in sequence order
+    int inc = n;  // inclusive scan over the lanes, in sequence order
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long v = __shfl_up_sync(0xffffffffu, inc, o);
+      const int v = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += v;
     }
-    const long long here = __shfl_sync(0xffffffffu, inc, 31);
+    const int here = __shfl_sync(0xffffffffu, inc, 31);
     if (r < here) {
       const int src = __ffs(__ballot_sync(0xffffffffu, r < inc)) - 1;
-      const long long idx = r - __shfl_sync(0xffffffffu, inc - n, src);
+      const int before = __shfl_sync(0xffffffffu, inc - n, src);
       const int q0 = __shfl_sync(0xffffffffu, f0, src);
-      return {src + 32 * j, q0 + (int)(idx / a.n_kv), (int)(idx % a.n_kv)};
+      const int cq = __shfl_sync(0xffffffffu, c00, src), lq = __shfl_sync(0xffffffffu, l00, src);
+      const int cl = __shfl_sync(0xffffffffu, cc[0], src);
+      // the sequence's cu_q and seq_lens entries when lane src holds them
+      // (sequences below 32), else cq0 = -1: the caller reads them
+      return {src + 32 * j, q0 + (r - before), g, j == 0 ? cq : -1, cl, lq};
     }
     r -= here;
   }
-  return {-1, 0, 0};  // not reached: the ranks below total cover every tile
+  return {-1, 0, 0, 0, 0, 0};  // not reached: the ranks below the total cover every pair
 }
 
 // Roles: eight softmax warps (one row per thread); lane 0 of one warp issues
@@ -258,11 +289,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
-  // ---- this block's tile: longest first; past kTRankSeqs sequences, the
-  // grid's own order (a sequence's latest tiles first)
+  // ---- this block's tile: longest first; past kTRankSeqs sequences (or
+  // 2^31 (sequence, query tile) pairs) the grid's own order, a sequence's
+  // latest tiles first
   const int cap = a.max_blocks * BS;
-  int s, qt, g;
-  if (a.num_seqs <= kTRankSeqs) {
+  int s, qt, g, cq0, c, L;
+  if (a.rank_tiles) {
     int* sel = reinterpret_cast<int*>(smem + C::SEL_OFF);
     if (warp == 0) {
       const long long rank =
@@ -272,49 +304,82 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
         sel[0] = t.s;
         sel[1] = t.qt;
         sel[2] = t.g;
+        sel[3] = t.cq0;
+        sel[4] = t.c;
+        sel[5] = t.L;
       }
     }
     __syncthreads();
     s = sel[0];
     qt = sel[1];
     g = sel[2];
+    cq0 = sel[3];
+    c = sel[4];
+    L = sel[5];
     if (s < 0) return;
+    if (cq0 < 0) {
+      cq0 = __ldg(&a.cu_q[s]);
+      c = __ldg(&a.cu_q[s + 1]) - cq0;
+      L = __ldg(&a.seq_lens[s]);
+    }
   } else {
     s = blockIdx.y;
     g = blockIdx.z;
     qt = a.n_tiles - 1 - (int)blockIdx.x;
+    cq0 = __ldg(&a.cu_q[s]);
+    c = __ldg(&a.cu_q[s + 1]) - cq0;
+    L = __ldg(&a.seq_lens[s]);
   }
-  const int cq0 = __ldg(&a.cu_q[s]);
-  const int c = __ldg(&a.cu_q[s + 1]) - cq0;
   const int G = a.group, TQ = a.tile_tokens;
   const int t0 = qt * TQ;
   // a chunk longer than max_q_len breaks the contract: flagged (rows beyond
   // the grid's n_tiles * TQ stay unwritten)
   if (qt == 0 && g == 0 && tid == 0 && c > a.max_q_len) report(a.err, PA_DEV_ERR_SEQ_LEN);
   if (c <= 0 || t0 >= c) return;
-  int L = __ldg(&a.seq_lens[s]);
   if (L > cap || L < c) {  // clamped / nothing visible: flagged, rows not written if L < c
     if (tid == 0 && qt == 0 && g == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
     if (L > cap) L = cap;
   }
   const int nt = min(TQ, c - t0);  // query tokens in this tile
 
-  // ---- this thread's row of the tile: token t = tid / G, head n = tid % G
-  const int rt = tid / G, rn = tid - rt * G;
-  const bool row_ok = softmax && tid < TQ * G && rt < nt && L >= c;
-  const int pos = row_ok ? L - c + t0 + rt : -1;  // -1: no key visible, row not written
-  const int64_t orow = row_ok ? ((int64_t)(cq0 + t0 + rt) * a.n_q + (int64_t)g * G + rn) : -1;
-
-  // ---- Q tile into shared memory (K-major, swizzled); absent rows are zero
-  if (softmax) {
-    const uint4* qr = reinterpret_cast<const uint4*>(a.q + (orow < 0 ? 0 : orow) * D);
+  // ---- row r of the tile: token t = r / G, head n = r % G; its row of q and
+  // out, or -1 (absent: past the chunk, or nothing visible). The first row
+  // is kept in shared memory for the output rather than in registers
+  // through the main loop.
+  const float inv_g = 1.f / (float)G;  // t = r / G in floats: exact for r < 256, G <= 64
+  auto row_of = [&](int r, int64_t orow0, int nrows) -> int64_t {
+    const int t = (int)(((float)r + 0.5f) * inv_g);
+    return r < nrows ? orow0 + (int64_t)t * a.n_q + (r - t * G) : -1;
+  };
+  constexpr int CPR = D / 8;  // 16-byte pieces per row
+  bool row_ok;
+  {
+    const int nrows = L >= c ? nt * G : 0;  // every head of tokens t0 .. t0+nt-1
+    const int64_t orow0 = (int64_t)(cq0 + t0) * a.n_q + (int64_t)g * G;
+    if (tid == 0) *reinterpret_cast<int64_t*>(smem + C::ROWS_OFF) = orow0;
+    row_ok = softmax && tid < nrows;  // this thread's row is row tid
+    // ---- Q tile into shared memory (K-major, swizzled); absent rows are
+    // zero. Consecutive threads take consecutive 16-byte pieces of a row, so
+    // each warp instruction reads whole rows.
+    if (softmax) {
+      constexpr int IT = kTTileRows * CPR / kTThreads;
+      uint4 v[IT];  // every load in flight before the first store
 #pragma unroll
-    for (int ch = 0; ch < D / 8; ++ch) {
-      const uint4 v = orow < 0 ? make_uint4(0, 0, 0, 0) : __ldg(&qr[ch]);
-      *reinterpret_cast<uint4*>(smem + C::Q_OFF + wg * C::QWG + (ch >> 3) * C::QHALF +
-                                swz128(lr, (ch & 7) * 8)) = v;
+      for (int it = 0; it < IT; ++it) {
+        const int i = it * kTThreads + tid, r = i / CPR, ch = i % CPR;
+        const int64_t orow = row_of(r, orow0, nrows);
+        v[it] = orow < 0 ? make_uint4(0, 0, 0, 0)
+                         : __ldg(reinterpret_cast<const uint4*>(a.q + orow * D) + ch);
+      }
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int i = it * kTThreads + tid, r = i / CPR, ch = i % CPR;
+        *reinterpret_cast<uint4*>(smem + C::Q_OFF + (r >> 7) * C::QWG + (ch >> 3) * C::QHALF +
+                                  swz128(r & 127, (ch & 7) * 8)) = v[it];
+      }
     }
   }
+  const int pos = row_ok ? L - c + t0 + tid / G : -1;  // -1: no key visible, row not written
   const int pmax = L - c + t0 + nt - 1;  // the tile's last position
   const int n_kv = pmax < 0 ? 0 : pmax / kTKv + 1;
   const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
@@ -612,6 +677,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       wait(pv_done, (n_kv - 1) & 1);
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t orow = row_ok ? *reinterpret_cast<const int64_t*>(smem + C::ROWS_OFF) +
+                                        (int64_t)(tid / G) * a.n_q + (tid % G)
+                                  : -1;
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
@@ -725,6 +793,7 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   if (tiles > 2147483647) return PA_ERR_INVALID_ARG;
   a.n_tiles = (int)tiles;
   a.max_q_len = max_q_len;
+  a.rank_tiles = num_seqs <= kTRankSeqs && tiles * num_seqs < ((int64_t)1 << 31);
   a.scale_log2 = scale * kTLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 64) return prefill_bs<64>(block_size, a, k_pool, v_pool, st);
