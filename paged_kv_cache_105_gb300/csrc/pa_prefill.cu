@@ -98,9 +98,10 @@ struct TCfg {
   static constexpr int K_OFF = Q_OFF + kTWarpgroups * QWG;
   static constexpr int V_OFF = K_OFF + kTStages * KV_BYTES;
   // fullK, fullV, emptyK, emptyV (one per stage); per warpgroup: S full,
-  // S free, P full, P V done; then the one-time start signal of warpgroup 1
+  // S free, P full, P V done; the one-time start signal of warpgroup 1; per
+  // warpgroup, Q stored
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
-  static constexpr int NBARS = 4 * kTStages + 4 * kTWarpgroups + 1;
+  static constexpr int NBARS = 4 * kTStages + 4 * kTWarpgroups + 1 + kTWarpgroups;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FAULT_OFF = TMEM_OFF + 8;
   static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g, cq0, c, L
@@ -286,6 +287,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   // s_full0 + 32 w + 0, 8, 16, 24
   const uint32_t s_full0 = emptyV + 8 * kTStages;
   const uint32_t go1 = s_full0 + 32 * kTWarpgroups;
+  const uint32_t q_full0 = go1 + 8;  // per warpgroup: its Q rows stored
 
   griddep_wait();  // the chunk's K/V come from the preceding cache write
 
@@ -296,9 +298,73 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   int s, qt, g, cq0, c, L;
   if (a.rank_tiles) {
     int* sel = reinterpret_cast<int*>(smem + C::SEL_OFF);
+    const long long rank =
+        blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    // Up to 32 sequences and one (sequence, query tile) pair per thread, the
+    // whole block ranks: thread p takes pair p (pairs in (s, qt) order) and
+    // counts the pairs that go before it, costlier or as costly and earlier;
+    // the one with as many as rank / n_kv before it is the block's. Else
+    // warp 0 searches (longest_first_tile). Scratch in the Q region, which
+    // is loaded only after this.
+    int* scr = reinterpret_cast<int*>(smem + C::Q_OFF);
+    int *qpre = scr, *sc = scr + 40, *sb = scr + 72, *sc0 = scr + 104, *slr = scr + 136;
+    int *cost = scr + 168, *npairs = cost + kTCtaThreads;
     if (warp == 0) {
-      const long long rank =
-          blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+      if (a.num_seqs <= 32) {
+        int Q = 0;
+        if (lane < a.num_seqs) {
+          const int q0 = __ldg(&a.cu_q[lane]), lraw = __ldg(&a.seq_lens[lane]);
+          const int cl = __ldg(&a.cu_q[lane + 1]) - q0;
+          Q = cl <= 0 ? 0 : min((cl - 1) / a.tile_tokens + 1, a.n_tiles);
+          sc[lane] = cl;
+          sb[lane] = min(max(lraw, 0), cap) - cl - 1;  // costs as the clamped length does
+          sc0[lane] = q0;
+          slr[lane] = lraw;
+        }
+        int inc = Q;  // inclusive scan: pairs of sequences 0 .. lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += v;
+        }
+        qpre[lane + 1] = inc;
+        if (lane == 0) qpre[0] = 0;
+        if (lane == 31) *npairs = inc;
+      } else if (lane == 0) {
+        *npairs = -1;
+      }
+    }
+    __syncthreads();
+    const int pairs = *npairs;
+    if (pairs >= 0 && pairs <= kTCtaThreads) {
+      const int pr = (int)(rank / a.n_kv);
+      int my_cost = 0, my_s = 0;
+      if (tid < pairs) {
+        while (qpre[my_s + 1] <= tid) ++my_s;
+        const int t0p = (tid - qpre[my_s]) * a.tile_tokens;
+        const int pm = sb[my_s] + t0p + min(a.tile_tokens, sc[my_s] - t0p);  // last position
+        my_cost = pm < 0 ? 0 : pm / kTKv + 1;
+        cost[tid] = my_cost;
+      }
+      if (tid == 0 && rank >= (long long)pairs * a.n_kv) sel[0] = -1;  // no tile left
+      __syncthreads();
+      if (tid < pairs) {
+        int before = 0;
+#pragma unroll 4
+        for (int u = 0; u < pairs; ++u) {
+          const int cu = cost[u];
+          before += (cu > my_cost) | ((cu == my_cost) & (u < tid));
+        }
+        if (before == pr && rank < (long long)pairs * a.n_kv) {
+          sel[0] = my_s;
+          sel[1] = tid - qpre[my_s];
+          sel[2] = (int)(rank % a.n_kv);
+          sel[3] = sc0[my_s];
+          sel[4] = sc[my_s];
+          sel[5] = slr[my_s];
+        }
+      }
+    } else if (warp == 0) {
       const TileSel t = longest_first_tile(a, cap, rank, lane);
       if (lane == 0) {
         sel[0] = t.s;
@@ -342,48 +408,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   }
   const int nt = min(TQ, c - t0);  // query tokens in this tile
 
-  // ---- row r of the tile: token t = r / G, head n = r % G; its row of q and
-  // out, or -1 (absent: past the chunk, or nothing visible). The first row
-  // is kept in shared memory for the output rather than in registers
-  // through the main loop.
-  const float inv_g = 1.f / (float)G;  // t = r / G in floats: exact for r < 256, G <= 64
-  auto row_of = [&](int r, int64_t orow0, int nrows) -> int64_t {
-    const int t = (int)(((float)r + 0.5f) * inv_g);
-    return r < nrows ? orow0 + (int64_t)t * a.n_q + (r - t * G) : -1;
-  };
-  constexpr int CPR = D / 8;  // 16-byte pieces per row
-  bool row_ok;
-  {
-    const int nrows = L >= c ? nt * G : 0;  // every head of tokens t0 .. t0+nt-1
-    const int64_t orow0 = (int64_t)(cq0 + t0) * a.n_q + (int64_t)g * G;
-    if (tid == 0) *reinterpret_cast<int64_t*>(smem + C::ROWS_OFF) = orow0;
-    row_ok = softmax && tid < nrows;  // this thread's row is row tid
-    // ---- Q tile into shared memory (K-major, swizzled); absent rows are
-    // zero. Consecutive threads take consecutive 16-byte pieces of a row, so
-    // each warp instruction reads whole rows.
-    if (softmax) {
-      constexpr int IT = kTTileRows * CPR / kTThreads;
-      uint4 v[IT];  // every load in flight before the first store
-#pragma unroll
-      for (int it = 0; it < IT; ++it) {
-        const int i = it * kTThreads + tid, r = i / CPR, ch = i % CPR;
-        const int64_t orow = row_of(r, orow0, nrows);
-        v[it] = orow < 0 ? make_uint4(0, 0, 0, 0)
-                         : __ldg(reinterpret_cast<const uint4*>(a.q + orow * D) + ch);
-      }
-#pragma unroll
-      for (int it = 0; it < IT; ++it) {
-        const int i = it * kTThreads + tid, r = i / CPR, ch = i % CPR;
-        *reinterpret_cast<uint4*>(smem + C::Q_OFF + (r >> 7) * C::QWG + (ch >> 3) * C::QHALF +
-                                  swz128(r & 127, (ch & 7) * 8)) = v[it];
-      }
-    }
-  }
+  const int nrows = L >= c ? nt * G : 0;  // rows present: every head of tokens t0 .. t0+nt-1
+  const bool row_ok = softmax && tid < nrows;  // this thread's row is row tid
   const int pos = row_ok ? L - c + t0 + tid / G : -1;  // -1: no key visible, row not written
   const int pmax = L - c + t0 + nt - 1;  // the tile's last position
   const int n_kv = pmax < 0 ? 0 : pmax / kTKv + 1;
   const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
+  if (tid == 0)  // the first output row, kept in shared memory for the output
+    *reinterpret_cast<int64_t*>(smem + C::ROWS_OFF) = (int64_t)(cq0 + t0) * a.n_q + (int64_t)g * G;
 
+  // ---- set-up; then the copy warp starts the first K/V tiles while the
+  // softmax warps load Q (q_full tells each issuer its warpgroup's Q is in)
   if (warp == 0) tc_alloc(sbase + C::TMEM_OFF, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < C::NBARS; ++i) mbar_init(fullK + 8 * i, 1);
@@ -394,12 +429,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     for (int w = 0; w < kTWarpgroups; ++w) {  // every thread of warpgroup w, once per tile
       mbar_init(s_full0 + 32 * w + 8, 128);
       mbar_init(s_full0 + 32 * w + 16, 128);
+      mbar_init(q_full0 + 8 * w, 128);  // and once: Q stored
     }
 
     *fault = 0;
     fence_mbarrier_init();
   }
-  fence_proxy_async_smem();  // Q (generic writes) before the MMAs read it
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -550,7 +585,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       // Warpgroup 1 starts once S_0(0) is done, so that the two warpgroups
       // run out of phase to begin with.
       if (w == 1 && n_kv > 0) wait(go1, 0);
-      if (n_kv > 0) issue_s(0);
+      if (n_kv > 0) {
+        wait(q_full0 + 8 * w, 0);  // this warpgroup's Q stored (used once)
+        issue_s(0);
+      }
       if (w == 0 && n_kv > 0) tc_commit(go1);  // used once: one phase
 #pragma unroll 1
       for (int kt = 0; kt < n_kv; ++kt) {
@@ -560,7 +598,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     }
     __syncwarp();
   } else {
-    // ---- the softmax warps: one row per thread, on warpgroup wg's barriers
+    // ---- the softmax warps: one row per thread, on warpgroup wg's barriers.
+    // First this warpgroup's rows of Q into shared memory (K-major,
+    // swizzled; absent rows zero): consecutive threads take consecutive
+    // 16-byte pieces of a row, every load in flight before the first store.
+    {
+      constexpr int CPR = D / 8;  // 16-byte pieces per row
+      const int64_t orow0 = *reinterpret_cast<const int64_t*>(smem + C::ROWS_OFF);
+      const float inv_g = 1.f / (float)G;  // r / G in floats: exact for r < 256, G <= 64
+      uint4 v[CPR];
+#pragma unroll
+      for (int it = 0; it < CPR; ++it) {
+        const int idx = it * kTRows + lr, r = wg * kTRows + idx / CPR, ch = idx % CPR;
+        const int tr = (int)(((float)r + 0.5f) * inv_g);
+        v[it] = r < nrows ? __ldg(reinterpret_cast<const uint4*>(
+                                      a.q + (orow0 + (int64_t)tr * a.n_q + (r - tr * G)) * D) +
+                                  ch)
+                          : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int it = 0; it < CPR; ++it) {
+        const int idx = it * kTRows + lr, rl = idx / CPR, ch = idx % CPR;
+        *reinterpret_cast<uint4*>(smem + C::Q_OFF + wg * C::QWG + (ch >> 3) * C::QHALF +
+                                  swz128(rl, (ch & 7) * 8)) = v[it];
+      }
+      fence_proxy_async_smem();  // generic writes before the MMAs read them
+      mbar_arrive(q_full0 + 8 * wg);
+    }
     const uint32_t tO = tmem + tmem_o_col(wg), tS = tmem + tmem_s_col(wg);
     const uint32_t tP = tmem + tmem_p_col(wg);
     const uint32_t s_full = s_full0 + 32 * wg, s_free = s_full + 8;
