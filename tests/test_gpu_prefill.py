@@ -130,6 +130,23 @@ def test_many_sequences_every_row(num_seqs):
     compare(out, ref, wl.name)
 
 
+def test_many_tiles_few_sequences_every_row():
+    # 32 sequences with more (sequence, query tile) pairs than threads in a
+    # block: the tiles are ranked by one warp, each lane trying its own cost
+    # (16 heads per kv head: 16-token query tiles, 10 to 16 per sequence)
+    ctx = [(7 * k) % 150 for k in range(32)]
+    ch = [150 + (37 * k) % 100 for k in range(32)]
+    wl = W.prefill_batch(ctx, ch, Hq=16, Hkv=1, d=64, seed=12, name="prefill-32seq-g16")
+    assert sum(-(-c // 16) for c in ch) > 352
+    vals_cpu = W.make_prefill_values(wl)
+    ref = oracle_prefill_threaded(wl, vals_cpu, np.array(
+        [(t, h) for t in range(wl.total_q) for h in range(wl.n_q_heads)], np.int32))
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
+    out, err = gpu_prefill(wl, vals)
+    assert err == 0
+    compare(out.reshape(-1, wl.head_dim), ref, wl.name)
+
+
 def test_short_max_q_len_is_flagged():
     wl = W.prefill_batch([10, 0], [40, 100], Hq=32, Hkv=8, d=64, seed=5)  # 64-token tiles
     vals_cpu = W.make_prefill_values(wl)
