@@ -103,7 +103,7 @@ struct TCfg {
   static constexpr int BAR_OFF = V_OFF + kTStages * KV_BYTES;
   static constexpr int NBARS = 4 * kTStages + 4 * kTWarpgroups + 1 + kTWarpgroups;
   static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
-  static constexpr int FAULT_OFF = TMEM_OFF + 8;
+  static constexpr int FAULT_OFF = TMEM_OFF + 8;  // fault flag, warpgroup 0's finished tiles
   static constexpr int SEL_OFF = FAULT_OFF + 8;  // the block's tile: s, qt, g, cq0, c, L
   static constexpr int ROWS_OFF = SEL_OFF + 24;  // its first output row
   static constexpr size_t SMEM = 1024 + ROWS_OFF + 16;
@@ -433,6 +433,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     }
 
     *fault = 0;
+    fault[1] = 0;  // softmax tiles finished by warpgroup 0 (its thread 0)
     fence_mbarrier_init();
   }
   tc_fence_before();
@@ -638,6 +639,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       const int st = kt % kTStages;
       const uint64_t tmask = tile_mask(kt, ids_nxt);
       if (kt + 1 < n_kv) tile_ids(kt + 1, ids_nxt);  // in flight during this tile
+      if (wg == 1) {
+        // Not ahead of warpgroup 0: a softmax starts after warpgroup 0's of the
+        // same tile, so the two stay apart and each one's softmax overlaps the
+        // other's MMAs (in step, both wait on the tensor cores together).
+        if (lane == 0) {
+          const uint64_t t_start = globaltimer_ns();
+          const uint64_t limit = *fault ? kTWaitAfterFaultNs : kTWaitNs;
+#pragma unroll 1
+          for (uint32_t it = 0; fault[1] < kt + 1; ++it)
+            if (it >= (1u << 28) || globaltimer_ns() - t_start > limit) {
+              report(a.err, PA_DEV_ERR_TIMEOUT);
+              *fault = 1;
+              break;
+            }
+        }
+        __syncwarp();
+      }
       wait(s_full, kt & 1);  // S(kt) is in TMEM
       tc_fence_after();
       // masked, lazy online softmax of this thread's row. Scores stay in raw
@@ -732,6 +750,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       if (tmask != ~0ull) fence_proxy_async_smem();  // zeroed rows before the MMA reads them
       tc_fence_before();
       mbar_arrive(p_full);
+      if (tid == 0) fault[1] = kt + 1;
     }
 
     // ---- normalise and write the rows
