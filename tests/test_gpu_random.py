@@ -1,7 +1,9 @@
 """Randomised GPU parity: seeded random batch shapes (sequence count and
 lengths, block size, head dim, GQA group, split mode, bf16 or fp8 cache)
 through the whole decode step, each against the fp64 oracle on every output
-and the pool bytes exactly. The seeds are fixed, so a failure reproduces."""
+and the pool bytes exactly; and seeded random chunked-prefill batches, every
+output row against the oracle. The seeds are fixed, so a failure
+reproduces."""
 import numpy as np
 import pytest
 import torch
@@ -63,3 +65,37 @@ def test_random_batches_fp8(seed):
     assert np.array_equal(vals["k_pool"].cpu().numpy(), kp)
     assert np.array_equal(vals["v_pool"].cpu().numpy(), vp)
     compare(out, ref, wl.name)
+
+
+def random_prefill_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    n = int(rng.integers(1, 41))  # up to 32: the block-wide or one-warp ranking; beyond: the search
+    ctx = rng.integers(0, 400, size=n)
+    ch = rng.integers(0, 200, size=n)
+    ch[rng.random(n) < 0.15] = 0  # some sequences without a chunk
+    if ch.max() == 0:
+        ch[0] = 1
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    while hkv * g > 16:
+        hkv //= 2
+    return dict(ctx=[int(x) for x in ctx], ch=[int(x) for x in ch], bs=int(rng.choice([8, 16, 32])),
+                d=int(rng.choice([64, 128])), hkv=hkv, hq=hkv * g, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_prefill_batches(seed):
+    # seeded random chunked-prefill batches (sequence count, contexts, chunk
+    # lengths with some empty, block size, head dim, group size), every output
+    # row against the oracle
+    from tests.test_gpu_prefill import gpu_prefill, oracle_prefill_threaded
+    c = random_prefill_case(seed)
+    wl = W.prefill_batch(c["ctx"], c["ch"], block_size=c["bs"], Hq=c["hq"], Hkv=c["hkv"],
+                         d=c["d"], seed=c["seed"], name=f"random-prefill-{seed}")
+    vals_cpu = W.make_prefill_values(wl)
+    rows = np.array([(t, h) for t in range(wl.total_q) for h in range(wl.n_q_heads)], np.int32)
+    ref = oracle_prefill_threaded(wl, vals_cpu, rows)
+    vals = {k: v.to(DEV) for k, v in vals_cpu.items()}
+    out, err = gpu_prefill(wl, vals)
+    assert err == 0
+    compare(out.reshape(-1, wl.head_dim), ref, wl.name)
