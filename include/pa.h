@@ -185,9 +185,12 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  * c_s = 1 for every s is decode; cu_q[s] = 0 history (seq_lens = c_s) is a
  * whole-prompt prefill.
  *
- *   out            bf16 [cu_q[num_seqs]][n_q_heads][head_dim]
- *   q              bf16 [cu_q[num_seqs]][n_q_heads][head_dim]
+ *   out            bf16 [total_q][n_q_heads][head_dim], 16-B aligned
+ *   q              bf16 [total_q][n_q_heads][head_dim], 16-B aligned
  *   cu_q           int32 [num_seqs + 1], non-decreasing, cu_q[0] = 0 (device)
+ *   total_q        rows (tokens) of q and out, >= cu_q[num_seqs]; a chunk
+ *                  reaching past it is flagged PA_DEV_ERR_SEQ_LEN and its
+ *                  rows past total_q are neither read nor written
  *   max_q_len      host bound of max_s c_s (sizes the grid); rows of a
  *                  longer chunk are not written and PA_DEV_ERR_SEQ_LEN is set
  *   n_q_heads / n_kv_heads  <= 64
@@ -201,9 +204,9 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  */
 pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* block_tables, const int32_t* seq_lens, const int32_t* cu_q,
-                     int num_seqs, int max_blocks_per_seq, int num_blocks, int n_q_heads,
-                     int n_kv_heads, int head_dim, int block_size, float scale, int max_q_len,
-                     int32_t* err_word, pa_stream_t stream);
+                     int num_seqs, int total_q, int max_blocks_per_seq, int num_blocks,
+                     int n_q_heads, int n_kv_heads, int head_dim, int block_size, float scale,
+                     int max_q_len, int32_t* err_word, pa_stream_t stream);
 
 /*
  * pa_reshape_and_cache — write new tokens' K/V into their pool slots.

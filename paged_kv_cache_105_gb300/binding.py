@@ -43,7 +43,7 @@ SIGNATURES = {
     "pa_reshape_and_cache_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, C.c_float,
                                       C.c_float, _vp, _vp]),
     "pa_copy_blocks_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
-    "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+    "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                         C.c_float, _i, _vp, _vp]),
     "pa_swap_blocks": (_i, [_vp, _vp, _vp, _vp, _vp, _i, C.c_size_t, _i, _i, _vp, _vp]),
     "pa_copy_host": (_i, [_vp, _vp, C.c_size_t, _vp]),
@@ -351,7 +351,8 @@ def pa_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q, scale, *, m
     if block_tables.shape[0] != S or cu_q.shape[0] != S + 1:
         raise ValueError("block_tables needs one row and cu_q one entry per sequence (+1)")
     st = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
-                          _ptr(seq_lens), _ptr(cu_q), S, block_tables.shape[1], NB, Hq, Hkv, D,
+                          _ptr(seq_lens), _ptr(cu_q), S, TQ, block_tables.shape[1], NB, Hq,
+                          Hkv, D,
                           bs, float(scale), int(max_q_len), _ptr(err_word), _stream(stream, dev))
     if st != PA_OK:
         raise PAError("pa_prefill", st)

@@ -34,7 +34,11 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -75,7 +79,8 @@ struct PrefillArgs {
   const int32_t* seq_lens;
   const int32_t* cu_q;
   int32_t* err;
-  int num_seqs, max_blocks, num_blocks, n_q, n_kv, group;
+  int num_seqs, total_q, max_blocks, num_blocks, n_q, n_kv, group;
+  int q_tma;        // 1: the copy warp loads Q by TMA (G a power of two), else the softmax warps
   int tile_tokens;  // query tokens per tile: 256 / G, rounded down
   int rank_tiles;   // 1: blocks take the tiles longest first (longest_first_tile)
   int n_tiles;      // grid.x: tiles of the longest chunk
@@ -268,7 +273,8 @@ __device__ TileSel longest_first_tile(const PrefillArgs& a, int cap, long long r
 template <int D, int BS>
 __global__ void __launch_bounds__(kTCtaThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+                  const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmq, const PrefillArgs a) {
   using C = TCfg<D, BS>;
   constexpr int NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
@@ -402,13 +408,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   // the grid's n_tiles * TQ stay unwritten)
   if (qt == 0 && g == 0 && tid == 0 && c > a.max_q_len) report(a.err, PA_DEV_ERR_SEQ_LEN);
   if (c <= 0 || t0 >= c) return;
-  if (L > cap || L < c) {  // clamped / nothing visible: flagged, rows not written if L < c
+  // clamped / nothing visible (rows not written if L < c) / the chunk runs
+  // past the rows of q and out (those rows are neither read nor written):
+  // flagged
+  if (L > cap || L < c || cq0 + c > a.total_q) {
     if (tid == 0 && qt == 0 && g == 0) report(a.err, PA_DEV_ERR_SEQ_LEN);
     if (L > cap) L = cap;
   }
   const int nt = min(TQ, c - t0);  // query tokens in this tile
+  const int nt_rows = max(0, min(nt, a.total_q - (cq0 + t0)));  // of them inside q and out
 
-  const int nrows = L >= c ? nt * G : 0;  // rows present: every head of tokens t0 .. t0+nt-1
+  const int nrows = L >= c ? nt_rows * G : 0;  // rows present: every head of these tokens
   const bool row_ok = softmax && tid < nrows;  // this thread's row is row tid
   const int pos = row_ok ? L - c + t0 + tid / G : -1;  // -1: no key visible, row not written
   const int pmax = L - c + t0 + nt - 1;  // the tile's last position
@@ -429,7 +439,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     for (int w = 0; w < kTWarpgroups; ++w) {  // every thread of warpgroup w, once per tile
       mbar_init(s_full0 + 32 * w + 8, 128);
       mbar_init(s_full0 + 32 * w + 16, 128);
-      mbar_init(q_full0 + 8 * w, 128);  // and once: Q stored
+      mbar_init(q_full0 + 8 * w, a.q_tma ? 1 : 128);  // and once: Q stored
     }
 
     *fault = 0;
@@ -481,6 +491,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
       prefetch_tensormap(&tmv);
     }
     const int bi = lane / C::KH, bh = lane % C::KH;  // this lane's box: block, half
+    // Q by TMA: warpgroup w's 128 rows are the G heads of tokens t0 + w 128/G
+    // .. of the tile, one box (64 columns, G heads, 128/G tokens) per
+    // 64-column half; rows past total_q read as zeros. Rows past the chunk
+    // but inside q are read and never written out.
+    if (a.q_tma && n_kv > 0 && lane == 0) {
+      prefetch_tensormap(&tmq);
+      for (int w = 0; w < kTWarpgroups; ++w) {
+        const uint32_t qb = q_full0 + 8 * w;
+        mbar_arrive_expect_tx(qb, C::QWG);
+#pragma unroll
+        for (int h = 0; h < C::KH; ++h)
+          tma_load_3d(sbase + C::Q_OFF + w * C::QWG + h * C::QHALF, &tmq, h * 64, g * G,
+                      cq0 + t0 + w * (kTRows / G), qb);
+      }
+    }
     auto box_id = [&](int kt) {
       const int tok = kt * kTKv + bi * C::ROWS;
       return (lane < NBOX && tok < L) ? __ldg(&table[tok / BS]) : -1;
@@ -600,10 +625,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
     __syncwarp();
   } else {
     // ---- the softmax warps: one row per thread, on warpgroup wg's barriers.
-    // First this warpgroup's rows of Q into shared memory (K-major,
-    // swizzled; absent rows zero): consecutive threads take consecutive
-    // 16-byte pieces of a row, every load in flight before the first store.
-    {
+    // First, for a group size that is not a power of two (its 128 rows are not
+    // whole tokens, so not one box), this warpgroup's rows of Q into shared
+    // memory (K-major, swizzled; absent rows zero): consecutive threads take
+    // consecutive 16-byte pieces of a row, every load in flight before the
+    // first store.
+    if (!a.q_tma) {
       constexpr int CPR = D / 8;  // 16-byte pieces per row
       const int64_t orow0 = *reinterpret_cast<const int64_t*>(smem + C::ROWS_OFF);
       const float inv_g = 1.f / (float)G;  // r / G in floats: exact for r < 256, G <= 64
@@ -788,17 +815,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
   if (warp == 0) tc_dealloc(tmem, kTmemCols);
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// q [total_q][n_q][D] in boxes of one warpgroup's 128 rows: 64 columns (128
+// bytes, the swizzle span), the G heads of a kv head, 128 / G tokens.
+static pa_status make_q_map(CUtensorMap* map, const void* q, int D, int n_q, int total_q, int G) {
+  auto fn = q_encode_fn();
+  if (!fn) return cuda_fail_msg("pa_prefill", "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n_q, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)n_q * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kTRows / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : cuda_fail_msg("pa_prefill", "cuTensorMapEncodeTiled failed");
+}
+
 template <int D, int BS>
 pa_status launch_prefill(PrefillArgs a, const void* k_pool, const void* v_pool,
                          cudaStream_t stream) {
   using C = TCfg<D, BS>;
   const int64_t rows = (int64_t)a.num_blocks * a.n_kv * BS;
-  CUtensorMap tmk, tmv;
+  CUtensorMap tmk, tmv, tmq;
   int k3 = 0, v3 = 0;  // 2-D maps: each 64-column half lands in its own slab
   pa_status st = make_pool_map(&tmk, k_pool, D, 2, rows, C::ROWS, false, &k3);
   if (st != PA_OK) return st;
   st = make_pool_map(&tmv, v_pool, D, 2, rows, C::ROWS, false, &v3);
   if (st != PA_OK) return st;
+  memset(&tmq, 0, sizeof(tmq));
+  if (a.q_tma) {
+    st = make_q_map(&tmq, a.q, D, a.n_q, a.total_q, a.group);
+    if (st != PA_OK) return st;
+  }
   auto kern = prefill_tc_kernel<D, BS>;
   static bool configured = false;
   if (!configured) {
@@ -817,7 +878,7 @@ pa_status launch_prefill(PrefillArgs a, const void* k_pool, const void* v_pool,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, tmq, a);
   return e == cudaSuccess ? PA_OK : cuda_fail("pa_prefill launch", e);
 }
 
@@ -838,11 +899,12 @@ using namespace pa;
 
 extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                 const int32_t* block_tables, const int32_t* seq_lens,
-                                const int32_t* cu_q, int num_seqs, int max_blocks_per_seq,
-                                int num_blocks, int n_q_heads, int n_kv_heads, int head_dim,
-                                int block_size, float scale, int max_q_len, int32_t* err_word,
-                                pa_stream_t stream) {
-  if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+                                const int32_t* cu_q, int num_seqs, int total_q,
+                                int max_blocks_per_seq, int num_blocks, int n_q_heads,
+                                int n_kv_heads, int head_dim, int block_size, float scale,
+                                int max_q_len, int32_t* err_word, pa_stream_t stream) {
+  if (num_seqs < 0 || num_seqs > 65535 || total_q < 0 || max_blocks_per_seq < 1 ||
+      num_blocks < 1 ||
       n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 || max_q_len < 0)
     return PA_ERR_INVALID_ARG;
   if (n_q_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -853,7 +915,7 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   if ((int64_t)num_blocks * n_kv_heads * block_size >= (int64_t)1 << 31)
     return PA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale == INFINITY) return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !cu_q)
     return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
@@ -866,6 +928,7 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   a.cu_q = cu_q;
   a.err = err_word;
   a.num_seqs = num_seqs;
+  a.total_q = total_q;
   a.max_blocks = max_blocks_per_seq;
   a.num_blocks = num_blocks;
   a.n_q = n_q_heads;
@@ -877,6 +940,7 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   a.n_tiles = (int)tiles;
   a.max_q_len = max_q_len;
   a.rank_tiles = num_seqs <= kTRankSeqs && tiles * num_seqs < ((int64_t)1 << 31);
+  a.q_tma = (G & (G - 1)) == 0;  // 128 rows are 128 / G whole tokens
   a.scale_log2 = scale * kTLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 64) return prefill_bs<64>(block_size, a, k_pool, v_pool, st);

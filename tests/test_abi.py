@@ -158,8 +158,8 @@ def test_prefill_and_swap_host_validation(L):
     p = 1 << 12
     f = L.pa_prefill
 
-    def pre(q=p, cu=p, S=2, Hq=8, Hkv=2, D=128, bs=16, maxq=64, scale=0.1):
-        return f(p, q, p, p, p, p, cu, S, 4, 8, Hq, Hkv, D, bs, scale, maxq, None, None)
+    def pre(q=p, cu=p, S=2, TQ=100, Hq=8, Hkv=2, D=128, bs=16, maxq=64, scale=0.1):
+        return f(p, q, p, p, p, p, cu, S, TQ, 4, 8, Hq, Hkv, D, bs, scale, maxq, None, None)
 
     assert pre(D=96) == UNS
     assert pre(bs=12) == UNS
@@ -170,6 +170,8 @@ def test_prefill_and_swap_host_validation(L):
     assert pre(S=0, q=None) == B.PA_OK
     assert pre(maxq=0, q=None) == B.PA_OK
     assert pre(maxq=-1) == INV
+    assert pre(TQ=-1) == INV
+    assert pre(TQ=0, q=None) == B.PA_OK            # no rows: nothing to do
     assert pre(scale=0.0) == INV                 # the softmax scale must be > 0
     assert pre(scale=-0.1) == INV
     s = L.pa_swap_blocks
